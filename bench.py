@@ -1,0 +1,458 @@
+"""Benchmark: MoE-layer forward tokens/s on GB300 through libmoe's C ABI.
+
+Default workload: the Mixtral-8x7B-shaped layer (T=4096 tokens, d=4096, E=8,
+k=2, f=14336, bf16 activations and experts, fp32 router and accumulation),
+seeded synthetic inputs.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+One JSON line is printed by rank 0.  `value` is whole-job tokens/s with the
+inputs resident in HBM (device-timed with CUDA events, per step, L2 flushed
+between steps); `e2e` is the same metric through moe_forward_host with the
+activations in pinned host memory (copies inside the timed region).
+For N > 1 (torchrun) every rank runs its own batch of T tokens on its own GPU
+(no data-path collective: tokens are independent), timing is the max over
+ranks, and `scaling` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; GEMM % tensor peak, permute/combine % HBM BW"
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 9  # logits, top-k, histogram, scan, scatter, gather, G1, G2, combine
+
+
+# --------------------------------------------------------------------------
+# multi-rank helpers (also exercised by the CPU gloo tests)
+# --------------------------------------------------------------------------
+def dist_env():
+    """(rank, local_rank, world_size) from the torchrun environment."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def aggregate_throughput(units_per_rank: int, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# --------------------------------------------------------------------------
+# measurement helpers
+# --------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7],
+                             "sw_power": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm_max = max(r["max"] for r in rows)
+        # "under load": samples whose power is within 30% of the run's peak power
+        pw = [r["power"] for r in rows if r["power"] is not None]
+        pmax = max(pw) if pw else None
+        loaded = [r for r in rows if pmax is None or (r["power"] or 0) >= 0.7 * pmax] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": sm_max,
+                "reasons": sorted(reasons), "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": pmax}
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# the CPU oracle (reference arm and the cpu_baseline field)
+# --------------------------------------------------------------------------
+def oracle_sample_tokens_per_s(inp, w, budget_s: float, max_tokens: int):
+    """Time the oracle's whole-layer forward on the first n tokens of the
+    workload, n sized to about `budget_s` seconds of host work.
+    Returns (tokens_per_s, n, seconds, threads)."""
+    import numpy as np
+    from oracle import oracle
+
+    x = inp["x"].float().cpu().numpy()
+    Wr = inp["Wr"].float().cpu().numpy()
+    Wgu = inp["Wgu"].float().cpu().numpy()
+    Wd = inp["Wd"].float().cpu().numpy()
+    bias = None if inp["bias"] is None else inp["bias"].float().cpu().numpy()
+    oracle.build()
+    n = min(max_tokens, 8)
+    t0 = time.perf_counter()
+    oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    dt = time.perf_counter() - t0
+    n = int(max(1, min(max_tokens, n * budget_s / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.moe_forward(np.ascontiguousarray(x[:n]), Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt, oracle.num_threads()
+
+
+def run_reference(args, w):
+    import torch
+    from oracle import oracle
+    from token_dispatch_grouped_fp32_gb300 import synth
+
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synth.make_inputs(w, device=gen_dev)
+    x = inp["x"].float().cpu().numpy()
+    Wr = inp["Wr"].float().cpu().numpy()
+    Wgu = inp["Wgu"].float().cpu().numpy()
+    Wd = inp["Wd"].float().cpu().numpy()
+    del inp["Wgu"], inp["Wd"]
+    bias = None if inp["bias"] is None else inp["bias"].float().cpu().numpy()
+    oracle.build()
+    # size each step to ~ args.ref_step_s seconds of host work
+    n = min(w.T, 4)
+    t0 = time.perf_counter()
+    oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    dt = time.perf_counter() - t0
+    n = int(max(1, min(w.T, n * args.ref_step_s / max(dt, 1e-6))))
+    for _ in range(args.warmup if args.ref_warmup else 0):
+        oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    times = []
+    for s in range(args.steps):
+        lo = (s * n) % max(1, w.T - n + 1)
+        xs = x[lo:lo + n]
+        t0 = time.perf_counter()
+        oracle.moe_forward(xs, Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+        times.append(time.perf_counter() - t0)
+    value = n * len(times) / sum(times)
+    threads = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} consecutive tokens of the workload per step "
+                                   f"(whole layer: route, dispatch, experts, combine)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: T={w.T} d={w.d} E={w.E} k={w.k} f={w.f} {w.dtype}, "
+                        f"renormalised top-k{', Zipf-skewed routing' if w.zipf else ''}",
+            "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "seed": w.seed,
+            "l2": "256 MiB L2 flush between timed steps (per-step working set "
+                  "also exceeds L2)"}
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from token_dispatch_grouped_fp32_gb300 import build as _build
+    from token_dispatch_grouped_fp32_gb300 import synth
+
+    rank, local_rank, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier()
+    from token_dispatch_grouped_fp32_gb300 import moe
+
+    dev = torch.device("cuda", local_rank)
+    wr = w.with_(seed=w.seed + 100 * rank) if world > 1 else w
+    inp = synth.make_inputs(wr, device=dev)
+    x, Wr, Wgu, Wd = inp["x"], inp["Wr"], inp["Wgu"], inp["Wd"]
+    bias = inp["bias"]
+    layer = moe.MoELayer(Wr, Wgu, Wd, w.k, bias, w.renorm)
+    T = w.T
+    cfg = layer.config(T)
+    ws = layer.workspace(T)
+    out = torch.empty_like(x)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_forward(cfg, x, Wr, bias, Wgu, Wd, out, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    moe.moe_last_device_error()
+
+    # ---- timed region: K steps of moe_forward, per-step events ----
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    moe.moe_last_device_error()
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
+    value = aggregate_throughput(T, world, ms / 1e3)
+
+    # ---- per-kernel breakdown: the same launch sequence through the
+    # component entry points, events between the calls ----
+    P = T * w.k
+    logits = torch.empty(T, w.E, dtype=torch.float32, device=dev)
+    idx = torch.empty(T, w.k, dtype=torch.int32, device=dev)
+    wt = torch.empty(T, w.k, dtype=torch.float32, device=dev)
+    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    pos = torch.empty(P, dtype=torch.int32, device=dev)
+    src = torch.empty(P, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(P, w.d, dtype=x.dtype, device=dev)
+    h_perm = torch.empty(P, w.f, dtype=x.dtype, device=dev)
+    y_perm = torch.empty(P, w.d, dtype=x.dtype, device=dev)
+    out2 = torch.empty_like(x)
+    dws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device=dev)
+    names = ["route", "dispatch", "grouped_swiglu", "combine"]
+
+    def parts(ev=None):
+        if ev: ev[0].record(stream)
+        moe.moe_route(cfg, x, Wr, bias, logits, idx, wt, stream=stream)
+        if ev: ev[1].record(stream)
+        moe.moe_dispatch(cfg, idx, x, counts, offsets, pos, src, x_perm, dws, stream=stream)
+        if ev: ev[2].record(stream)
+        moe.moe_grouped_swiglu(cfg, x_perm, offsets, Wgu, Wd, h_perm, y_perm, stream=stream)
+        if ev: ev[3].record(stream)
+        moe.moe_combine(cfg, y_perm, pos, wt, out2, stream=stream)
+        if ev: ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        parts()
+    torch.cuda.synchronize()
+    per = {n: [] for n in names}
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        parts(ev)
+        torch.cuda.synchronize()
+        for j, n in enumerate(names):
+            per[n].append(ev[j].elapsed_time(ev[j + 1]))
+    same_as_fused = bool(torch.equal(out, out2))
+    kms = {n: sum(v) / len(v) for n, v in per.items()}
+
+    peaks = measured_peaks()
+    es = 2 if w.dtype == "bf16" else 4
+    gemm_flops = 6.0 * P * w.d * w.f
+    gemm_tflops = gemm_flops / (kms["grouped_swiglu"] * 1e-3) / 1e12
+    # minimal HBM bytes of the bandwidth kernels
+    disp_bytes = T * w.d * es + P * w.d * es + P * 4 * 4
+    comb_bytes = P * w.d * es + P * 8 + T * w.d * es
+    route_bytes = T * w.d * es + T * w.E * 4 * 2 + P * 8
+    hbm = peaks["hbm_gbs"]
+    kernels = {
+        "route": {"ms": kms["route"], "GB/s": route_bytes / kms["route"] / 1e6},
+        "dispatch": {"ms": kms["dispatch"], "GB/s": disp_bytes / kms["dispatch"] / 1e6,
+                     "frac_hbm": disp_bytes / kms["dispatch"] / 1e6 / hbm},
+        "grouped_swiglu": {"ms": kms["grouped_swiglu"], "TFLOP/s": gemm_tflops,
+                           "frac_tensor": gemm_tflops / peaks["bf16_tflops"]},
+        "combine": {"ms": kms["combine"], "GB/s": comb_bytes / kms["combine"] / 1e6,
+                    "frac_hbm": comb_bytes / kms["combine"] / 1e6 / hbm},
+        "sum_ms": sum(kms.values()), "same_output_as_moe_forward": same_as_fused,
+    }
+    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
+                "traffic": recorded_traffic(w), "kernel": "grouped_gemm_tc_kernel (G1 gate/up "
+                "+ SwiGLU, G2 down) via moe_grouped_swiglu",
+                "algorithmic": f"6*P*d*f = {gemm_flops:.4g} FLOP per call (P=T*k={P})",
+                "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+
+    # ---- e2e: activations in pinned host memory, copies inside the region ----
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+    out_dev = torch.empty_like(x)
+
+    def e2e_step():
+        moe.moe_forward_host(cfg, x_host, Wr, bias, Wgu, Wd, out_host, x_dev, out_dev, ws,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dev)
+    moe.moe_last_device_error()
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            tps, n, secs, thr = oracle_sample_tokens_per_s(inp, w, args.cpu_budget_s, T)
+            cpu = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                   "sample": f"first {n} tokens of the workload, whole layer "
+                             f"(route, dispatch, experts, combine), {secs:.1f} s"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic", "config": workload_config(w),
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
+            "e2e": {"value": aggregate_throughput(T, world, e2e / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * w.d * es, "d2h_bytes_per_step": T * w.d * es},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks.summary(), "wall_s_timed_region": t_wall,
+        }
+        print(json.dumps(line), flush=True)
+    barrier()
+    if world > 1 and dist.is_initialized():
+        dist.destroy_process_group()
+    return line
+
+
+def recorded_traffic(w):
+    """DRAM bytes per moe_grouped_swiglu call from the committed ncu summary,
+    if it was taken on this workload with the current kernel source."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "grouped_gemm_tc_traffic.json")
+    src = os.path.join(ROOT, "token_dispatch_grouped_fp32_gb300", "csrc", "gemm_tc.cu")
+    if not (os.path.exists(p) and os.path.exists(src)):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh)
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if rec.get("gemm_tc_sha256") != digest:
+        return None
+    return rec.get("per_call_bytes", {}).get(w.name)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixtral")
+    ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--ref-warmup", action="store_true",
+                    help="run the warm-up steps in the reference arm too")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from token_dispatch_grouped_fp32_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.tokens:
+        w = w.with_tokens(args.tokens)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,110 @@
+"""The C ABI library loads and exports what include/moe.h declares; host-side
+argument checks and workspace queries behave as documented (no GPU needed:
+every call here returns before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from token_dispatch_grouped_fp32_gb300 import build
+    build.build()
+    from token_dispatch_grouped_fp32_gb300 import moe as _moe
+    return _moe
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(moe):
+    names = _declared_functions()
+    assert len(names) >= 12
+    lib = ctypes.CDLL(moe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(moe):
+    for code, name in [(0, "MOE_OK"), (-1, "MOE_ERR_INVALID_ARG"), (-2, "MOE_ERR_UNSUPPORTED"),
+                       (-3, "MOE_ERR_WORKSPACE"), (-4, "MOE_ERR_CUDA"),
+                       (-5, "MOE_ERR_DEVICE_TIMEOUT"), (-6, "MOE_ERR_BAD_ROUTING")]:
+        assert moe.moe_status_string(code) == name
+
+
+def test_workspace_sizes(moe):
+    cfg = moe.config(4096, 4096, 8, 2, 14336, "bf16")
+    ws = moe.moe_workspace_size(cfg)
+    P = 4096 * 2
+    perm = 2 * P * (4096 + 14336 + 4096)
+    assert perm <= ws <= perm + 4096 * 8 * 4 + 10 * P * 4 + 64 * 1024
+    assert moe.moe_workspace_size(moe.config(0, 4096, 8, 2, 14336)) == 0
+    assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * ((P + 2047) // 2048)
+    # invalid config -> 0
+    assert moe.moe_workspace_size(moe.config(4, 4096, 8, 9, 14336)) == 0
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=-1), dict(d=0), dict(f=0), dict(E=0), dict(k=0), dict(k=9), dict(d=12), dict(f=20),
+    dict(T=2 ** 29, k=8),
+])
+def test_bad_config_rejected_before_launch(moe, bad):
+    base = dict(T=16, d=64, E=8, k=2, f=64)
+    base.update(bad)
+    cfg = moe.config(base["T"], base["d"], base["E"], base["k"], base["f"])
+    st = moe.moe_combine(cfg, 16, 16, 16, 16, stream=0, raise_on_error=False)
+    assert st == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_last_error_message()
+
+
+def test_unsupported_shapes(moe):
+    cfg = moe.config(16, 64, 2048, 2, 64)
+    assert moe.moe_combine(cfg, 16, 16, 16, 16, stream=0, raise_on_error=False) == \
+        moe.MOE_ERR_UNSUPPORTED
+    cfg = moe.config(16, 64, 8, 2, 64, dtype=7)
+    assert moe.moe_combine(cfg, 16, 16, 16, 16, stream=0, raise_on_error=False) == \
+        moe.MOE_ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers(moe):
+    cfg = moe.config(16, 64, 8, 2, 64)
+    assert moe.moe_combine(cfg, None, 16, 16, 16, stream=0, raise_on_error=False) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_combine(cfg, 16, 16, 16, 24, stream=0, raise_on_error=False) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_forward(cfg, 16, 16, None, 16, 16, None, 16, 1 << 30, stream=0,
+                           raise_on_error=False) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_too_small(moe):
+    cfg = moe.config(16, 64, 8, 2, 64)
+    need = moe.moe_workspace_size(cfg)
+    st = moe.moe_forward(cfg, 16, 16, None, 16, 16, 16, 16, need - 1, stream=0,
+                         raise_on_error=False)
+    assert st == moe.MOE_ERR_WORKSPACE
+    st = moe.moe_dispatch(cfg, 16, 16, 16, 16, 16, 16, 16, 16, 3, stream=0, raise_on_error=False)
+    assert st == moe.MOE_ERR_WORKSPACE
+
+
+def test_empty_batch_is_a_no_op(moe):
+    cfg = moe.config(0, 64, 8, 2, 64)
+    assert moe.moe_forward(cfg, 16, 16, None, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
+    assert moe.moe_route(cfg, 16, 16, None, 16, 16, 16, stream=0) == moe.MOE_OK
+    assert moe.moe_dispatch(cfg, 16, 16, 16, 16, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
+    assert moe.moe_grouped_swiglu(cfg, 16, 16, 16, 16, 16, 16, stream=0) == moe.MOE_OK
+    assert moe.moe_combine(cfg, 16, 16, 16, 16, stream=0) == moe.MOE_OK
+
+
+def test_raises_with_detail(moe):
+    cfg = moe.config(16, 64, 8, 2, 64)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_combine(cfg, None, 16, 16, 16, stream=0)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+    assert "NULL" in str(ei.value)

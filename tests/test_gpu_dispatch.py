@@ -1,0 +1,84 @@
+"""Dispatch parity: counts, offsets, the permutation and its inverse bit-exact
+against the oracle; the permuted rows are byte copies of the token rows."""
+import numpy as np
+import pytest
+import torch
+
+from token_dispatch_grouped_fp32_gb300 import synth
+from tests.gpu_util import load_moe
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return load_moe()
+
+
+def _routing(oracle, T, E, k, seed, skew=0.0):
+    L = synth.make_logits(T, E, seed).numpy()
+    if skew:
+        L = L + skew * (np.arange(E, dtype=np.float32) == 3)[None, :]
+    idx, _ = oracle.topk(L, k, True)
+    return idx
+
+
+def _run_dispatch(moe, idx, x, E):
+    T, k = idx.shape
+    d = x.shape[1]
+    cfg = moe.config(T, d, E, k, 8, x.dtype)
+    P = T * k
+    dev = "cuda"
+    counts = torch.full((E,), -1, dtype=torch.int32, device=dev)
+    offsets = torch.full((E + 1,), -1, dtype=torch.int32, device=dev)
+    pos = torch.full((P,), -1, dtype=torch.int32, device=dev)
+    src = torch.full((P,), -1, dtype=torch.int32, device=dev)
+    x_perm = torch.zeros(P, d, dtype=x.dtype, device=dev)
+    ws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device=dev)
+    moe.moe_dispatch(cfg, torch.from_numpy(idx).cuda(), x.cuda(), counts, offsets, pos, src,
+                     x_perm, ws)
+    torch.cuda.synchronize()
+    return counts.cpu().numpy(), offsets.cpu().numpy(), pos.cpu().numpy(), src.cpu().numpy(), \
+        x_perm.cpu()
+
+
+DISPATCH_CASES = [
+    # T, E, k, d, dtype, skew
+    (1, 8, 2, 64, torch.bfloat16, 0.0),
+    (100, 8, 2, 64, torch.bfloat16, 0.0),
+    (3000, 8, 2, 64, torch.float32, 0.0),      # 3 chunks, ragged tail
+    (5000, 128, 8, 32, torch.bfloat16, 0.0),   # 20 chunks
+    (2049, 1, 1, 16, torch.bfloat16, 0.0),     # single expert
+    (1000, 64, 6, 24, torch.bfloat16, 0.0),
+    (4000, 16, 2, 8, torch.bfloat16, 50.0),    # one expert takes every token
+    (6000, 1024, 8, 8, torch.bfloat16, 0.0),   # many experts, most empty per chunk
+    (300000, 16, 8, 8, torch.bfloat16, 0.0),   # 2.4M pairs: chunks grow past 2048
+]
+
+
+@pytest.mark.parametrize("T,E,k,d,dtype,skew", DISPATCH_CASES)
+def test_dispatch_matches_oracle(moe, oracle, T, E, k, d, dtype, skew):
+    idx = _routing(oracle, T, E, k, 77 + T + E, skew)
+    g = torch.Generator().manual_seed(T)
+    x = torch.randn(T, d, generator=g).to(dtype)
+    counts, offsets, pos, src, x_perm = _run_dispatch(moe, idx, x, E)
+    rc, ro, rp, rs = oracle.dispatch(idx, E)
+    np.testing.assert_array_equal(counts, rc)
+    np.testing.assert_array_equal(offsets, ro)
+    np.testing.assert_array_equal(pos, rp)
+    np.testing.assert_array_equal(src, rs)
+    # rows are byte copies of the token rows
+    assert torch.equal(x_perm, x[torch.from_numpy(rs).long()])
+
+
+def test_dispatch_flags_out_of_range_expert(moe, oracle):
+    T, E, k = 50, 8, 2
+    idx = _routing(oracle, T, E, k, 5)
+    idx[7, 1] = E + 3
+    x = torch.randn(T, 16).to(torch.bfloat16)
+    moe.moe_last_device_error(raise_on_error=False)  # clear
+    counts, offsets, pos, src, _ = _run_dispatch(moe, idx, x, E)
+    assert moe.moe_last_device_error(raise_on_error=False) == moe.MOE_ERR_BAD_ROUTING
+    assert counts.sum() == T * k - 1 and offsets[-1] == T * k - 1
+    assert pos[7 * k + 1] == -1
+    assert moe.moe_last_device_error(raise_on_error=False) == moe.MOE_OK  # cleared

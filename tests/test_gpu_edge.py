@@ -1,0 +1,94 @@
+"""Edge cases and properties of the layer on the GPU: a single token, one
+expert, k = E without renormalisation, every token on one expert, an empty
+batch, determinism, CUDA-graph capture, and the host-buffer entry point."""
+import pytest
+import torch
+
+from token_dispatch_grouped_fp32_gb300 import synth
+from tests.gpu_util import check_layer, load_moe
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return load_moe()
+
+
+def test_single_token_decode(moe, oracle):
+    w = synth.WORKLOADS["gptoss_decode"].with_tokens(1)
+    check_layer(moe, oracle, w)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_one_expert(moe, oracle, dtype):
+    w = synth.Workload("one", 300, 128, 1, 1, 264, dtype, 21)
+    check_layer(moe, oracle, w, device="cpu")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_k_equals_E_without_renorm(moe, oracle, dtype):
+    w = synth.Workload("dense", 200, 96, 4, 4, 136, dtype, 22, renorm=False)
+    check_layer(moe, oracle, w, device="cpu")
+
+
+def test_every_token_on_one_expert(moe, oracle):
+    w = synth.Workload("hot", 700, 128, 16, 2, 256, "bf16", 23)
+    bias = torch.zeros(16)
+    bias[5] = 100.0
+    check_layer(moe, oracle, w, device="cpu", bias=bias)
+
+
+def _layer(moe, name, T):
+    w = synth.WORKLOADS[name].with_tokens(T)
+    inp = synth.make_inputs(w, device="cuda")
+    layer = moe.MoELayer(inp["Wr"], inp["Wgu"], inp["Wd"], w.k,
+                         None if inp["bias"] is None else inp["bias"], w.renorm)
+    return layer, inp["x"]
+
+
+def test_empty_batch(moe):
+    layer, x = _layer(moe, "qwen3_zipf", 16)
+    out = layer(x[:0])
+    assert out.shape == (0, x.shape[1])
+
+
+def test_deterministic(moe):
+    layer, x = _layer(moe, "qwen3_zipf", 3000)
+    a = layer(x).clone()
+    b = layer(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_cuda_graph_capture(moe):
+    layer, x = _layer(moe, "gptoss_prefill", 1000)
+    ref = layer(x).clone()
+    out = torch.empty_like(x)
+    layer.workspace(x.shape[0])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer(x, out=out)  # warm up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    out.zero_()
+    with torch.cuda.graph(g):
+        layer(x, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+def test_forward_host_buffers(moe):
+    layer, x = _layer(moe, "mixtral", 256)
+    ref = layer(x).clone()
+    cfg = layer.config(x.shape[0])
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(x)
+    out_dev = torch.empty_like(x)
+    moe.moe_forward_host(cfg, x_host, layer.Wr, layer.logit_bias, layer.W_gate_up, layer.W_down,
+                         out_host, x_dev, out_dev, layer.workspace(x.shape[0]))
+    torch.cuda.synchronize()
+    assert torch.equal(out_host, ref.cpu())

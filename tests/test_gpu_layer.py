@@ -1,0 +1,43 @@
+"""Whole-layer parity of moe_forward against the oracle.
+
+Small cases compare every token.  The benchmark workloads run at their full
+sizes in the same launch configuration the benchmark times; there the oracle
+computes a sample of tokens one by one (its weights are the float images of
+the touched experts only).  Tokens whose oracle routing has a near tie at the
+selection boundary (a flip fp32 rounding can cause) are excluded from the
+output comparison after the tie is confirmed."""
+import pytest
+
+from token_dispatch_grouped_fp32_gb300 import synth
+from tests.gpu_util import check_layer, load_moe
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return load_moe()
+
+
+def test_layer_tiny_fp32_all_tokens(moe, oracle):
+    assert check_layer(moe, oracle, synth.WORKLOADS["tiny_fp32"], device="cpu") >= 60
+
+
+def test_layer_tiny_bf16_all_tokens(moe, oracle):
+    w = synth.WORKLOADS["tiny_fp32"].with_(dtype="bf16")
+    assert check_layer(moe, oracle, w, device="cpu") >= 60
+
+
+@pytest.mark.parametrize("name,T", [("mixtral", 333), ("qwen3_zipf", 211), ("gptoss_decode", 64)])
+def test_layer_reduced_batch_all_tokens(moe, oracle, name, T):
+    w = synth.WORKLOADS[name].with_tokens(T)
+    check_layer(moe, oracle, w, sample=None if w.E <= 8 else 40, max_experts=64)
+
+
+@pytest.mark.parametrize("name,sample", [("mixtral", 24), ("gptoss_decode", 12),
+                                         ("gptoss_prefill", 12), ("qwen3_zipf", 12),
+                                         ("deepseek", 5)])
+def test_layer_full_size_sampled(moe, oracle, name, sample):
+    w = synth.WORKLOADS[name]
+    n = check_layer(moe, oracle, w, sample=sample, max_experts=40)
+    assert n >= 3

@@ -1,0 +1,85 @@
+"""Router parity: top-k indices bit-exact and weights within the fp32 bound
+against the oracle on the same fp32 logit buffer; router logits within the
+fp32 summation bound."""
+import numpy as np
+import pytest
+import torch
+
+from token_dispatch_grouped_fp32_gb300 import synth
+from tests.gpu_util import f32, load_moe, logit_tolerance, near_tie, weight_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    return load_moe()
+
+
+ROUTE_CASES = [
+    # T, E, k, ties
+    (1, 8, 2, None),
+    (37, 8, 2, None),
+    (4096, 8, 2, None),
+    (4096, 8, 2, "coarse"),
+    (513, 128, 4, None),
+    (777, 128, 8, "coarse"),
+    (300, 256, 8, None),
+    (300, 256, 8, "coarse"),
+    (100, 33, 5, None),
+    (64, 1024, 32, None),
+    (200, 3, 3, None),
+    (50, 64, 6, "all_equal"),
+    (8192, 256, 8, None),
+]
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+@pytest.mark.parametrize("T,E,k,ties", ROUTE_CASES)
+def test_route_from_logits_matches_oracle(moe, oracle, T, E, k, ties, renorm):
+    L = synth.make_logits(T, E, 1000 + T + E, ties=ties)
+    cfg = moe.config(T, 8, E, k, 8, "f32", renorm)
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), -7.0, dtype=torch.float32, device="cuda")
+    moe.moe_route_from_logits(cfg, L.cuda(), idx, w)
+    torch.cuda.synchronize()
+    ref_idx, ref_w = oracle.topk(L.numpy(), k, renorm)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    err = np.abs(w.cpu().numpy().astype(np.float64) - ref_w).max()
+    assert err <= weight_tolerance(E), err
+
+
+@pytest.mark.parametrize("name,T", [("tiny_fp32", 64), ("mixtral", 512), ("gptoss_prefill", 700),
+                                    ("qwen3_zipf", 1500), ("deepseek", 300)])
+def test_route_logits_and_selection(moe, oracle, name, T):
+    w = synth.WORKLOADS[name].with_tokens(T)
+    inp = synth.make_inputs(w, weights=False)
+    x, Wr, bias = inp["x"], inp["Wr"], inp["bias"]
+    cfg = moe.config(T, w.d, w.E, w.k, w.f, w.torch_dtype, w.renorm)
+    logits = torch.empty(T, w.E, dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, w.k, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, w.k, dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, x.cuda(), Wr.cuda(), None if bias is None else bias.cuda(), logits, idx, wt)
+    torch.cuda.synchronize()
+    xs, Wrs = f32(x), f32(Wr)
+    bs = None if bias is None else f32(bias)
+    ref_L = oracle.router_logits(xs, Wrs, bs)
+    tol = logit_tolerance(xs, Wrs, bs)
+    gL = logits.cpu().numpy()
+    assert (np.abs(gL.astype(np.float64) - ref_L) <= tol).all()
+
+    # moe_route selects on exactly the logits it wrote
+    idx2 = torch.empty_like(idx)
+    w2 = torch.empty_like(wt)
+    moe.moe_route_from_logits(cfg, logits, idx2, w2)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx2) and torch.equal(wt, w2)
+
+    # against the oracle's own routing: equal except where a near tie may flip
+    ref_idx, ref_w = oracle.topk(ref_L, w.k, w.renorm)
+    g_idx = idx.cpu().numpy()
+    differ = np.nonzero((g_idx != ref_idx).any(1))[0]
+    for t in differ:
+        assert near_tie(ref_L[t], w.k, tol[t]) or \
+            sorted(g_idx[t].tolist()) == sorted(ref_idx[t].tolist()), t
+    assert len(differ) <= max(2, T // 200)

@@ -1,0 +1,216 @@
+// dispatch.cu -- token dispatch on one device: per-expert histogram, exclusive
+// scan, stable scatter into expert-contiguous order, and the row gather.
+//
+// Transformers docs "Expert parallelism", section "Token dispatch": every
+// (token, expert) pair is sent to its expert and the experts run on the rows
+// they receive.  On one GPU "sending" is a permutation: pair (t, j) gets row
+// pos[t*k+j] of its expert's segment, segments laid out in expert order.
+//
+// Stability: pairs are cut into chunks of consecutive pair ids; chunk b's
+// rows for expert e start at the exclusive scan of the expert-major
+// [E][chunks] count matrix, and inside a chunk every warp ranks its pairs
+// with __match_any_sync in pair order.  So rows of one expert are in
+// ascending pair id, hence ascending token id, with no atomics deciding order.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// counts of chunk b, stored expert-major: hist[e * NB + b]
+__global__ void __launch_bounds__(kThreads)
+chunk_histogram_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB,
+                       int32_t *__restrict__ hist, DevStatus ds) {
+    extern __shared__ int sh_count[];
+    for (int e = threadIdx.x; e < E; e += kThreads) sh_count[e] = 0;
+    __syncthreads();
+    const int64_t q0 = (int64_t)blockIdx.x * chunk;
+    const int64_t q1 = min(q0 + chunk, P);
+    for (int64_t q = q0 + threadIdx.x; q < q1; q += kThreads) {
+        int e = idx[q];
+        if ((unsigned)e < (unsigned)E)
+            atomicAdd(&sh_count[e], 1);
+        else
+            raise_error(ds, kErrBadRouting);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) hist[(int64_t)e * NB + blockIdx.x] = sh_count[e];
+}
+
+// Single block: exclusive scan of hist[0 .. E*NB) in place (the base row of
+// every (expert, chunk)), then counts[e] and offsets[0..E].
+constexpr int kScanThreads = 1024;
+__global__ void __launch_bounds__(kScanThreads)
+scan_kernel(int32_t *__restrict__ hist, int E, int NB, int32_t *__restrict__ counts,
+            int32_t *__restrict__ offsets) {
+    __shared__ int warp_tot[kScanThreads / 32];
+    __shared__ int total_s;
+    const int n = E * NB;
+    const int seg = (n + kScanThreads - 1) / kScanThreads;
+    const int beg = min(n, (int)threadIdx.x * seg);
+    const int end = min(n, beg + seg);
+    int local = 0;
+    for (int i = beg; i < end; ++i) local += hist[i];
+    // block exclusive scan of `local`
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int v = warp_tot[lane];
+        int inc = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int u = __shfl_up_sync(0xffffffffu, inc, off);
+            if (lane >= off) inc += u;
+        }
+        warp_tot[lane] = inc - v;  // exclusive warp base
+        if (lane == 31) total_s = inc;
+    }
+    __syncthreads();
+    int run = warp_tot[wid] + incl - local;
+    for (int i = beg; i < end; ++i) {
+        int c = hist[i];
+        hist[i] = run;
+        run += c;
+    }
+    __syncthreads();
+    const int total = total_s;
+    for (int e = threadIdx.x; e < E; e += kScanThreads) {
+        int b0 = hist[e * NB];
+        int b1 = (e + 1 < E) ? hist[(e + 1) * NB] : total;
+        offsets[e] = b0;
+        counts[e] = b1 - b0;
+    }
+    if (threadIdx.x == 0) offsets[E] = total;
+}
+
+// Stable scatter: warp w of block b ranks pairs [q0 + w*sub, q0 + (w+1)*sub).
+__global__ void __launch_bounds__(kThreads)
+scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chunk, int NB,
+               const int32_t *__restrict__ base, int32_t *__restrict__ pos,
+               int32_t *__restrict__ src_token) {
+    extern __shared__ int sh_warp[];  // [kWarps][E]: per-warp counts, then running row
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) sh_warp[i] = 0;
+    __syncthreads();
+    const int sub = chunk / kWarps;  // multiple of 32
+    const int64_t w0 = (int64_t)blockIdx.x * chunk + (int64_t)wid * sub;
+    const int64_t w1 = min(w0 + sub, P);
+    int *mine = sh_warp + wid * E;
+    for (int64_t q = w0 + lane; q < w1; q += 32) {
+        int e = idx[q];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int run = base[(int64_t)e * NB + blockIdx.x];
+        for (int w = 0; w < kWarps; ++w) {
+            int c = sh_warp[w * E + e];
+            sh_warp[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t qb = w0; qb < w1; qb += 32) {  // warp-uniform trip count
+        const int64_t q = qb + lane;
+        int e = -1;
+        if (q < w1) {
+            e = idx[q];
+            if ((unsigned)e >= (unsigned)E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt_mask);
+        const int row0 = (e >= 0) ? mine[e] : 0;
+        __syncwarp();
+        if (q < w1) {
+            if (e >= 0) {
+                const int row = row0 + rank;
+                pos[q] = row;
+                src_token[row] = (int32_t)(q / k);
+                if (lane == 31 - __clz(peers)) mine[e] = row0 + __popc(peers);
+            } else {
+                pos[q] = -1;  // dropped pair (expert id out of range)
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Row gather x_perm[pos[q]] = x[q / k]: one warp per pair, 16-byte vectors.
+__global__ void __launch_bounds__(kThreads)
+gather_rows_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ pos, int64_t P,
+                   int k, int row_vecs, uint8_t *__restrict__ x_perm) {
+    const int lane = threadIdx.x & 31;
+    const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (q >= P) return;
+    const int row = pos[q];
+    if (row < 0) return;
+    const int64_t t = q / k;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x) + t * row_vecs;
+    uint4 *dst = reinterpret_cast<uint4 *>(x_perm) + (int64_t)row * row_vecs;
+    int i = lane;
+    for (; i + 96 < row_vecs; i += 128) {
+        uint4 a = ldg16(src + i), b = ldg16(src + i + 32), c = ldg16(src + i + 64),
+              d = ldg16(src + i + 96);
+        stg16(dst + i, a);
+        stg16(dst + i + 32, b);
+        stg16(dst + i + 64, c);
+        stg16(dst + i + 96, d);
+    }
+    for (; i < row_vecs; i += 32) stg16(dst + i, ldg16(src + i));
+}
+
+}  // namespace
+
+DispatchGrid dispatch_grid(int64_t P) {
+    DispatchGrid g;
+    g.chunk = 2048;
+    int64_t nb = (P + g.chunk - 1) / g.chunk;
+    if (nb > 1024) {
+        int64_t c = (P + 1023) / 1024;
+        c = (c + 255) / 256 * 256;
+        g.chunk = (int)c;
+        nb = (P + c - 1) / c;
+    }
+    g.blocks = (int)(nb < 1 ? 1 : nb);
+    return g;
+}
+
+size_t dispatch_scratch_bytes(const Shape &s) {
+    DispatchGrid g = dispatch_grid(s.P());
+    return sizeof(int32_t) * (size_t)s.E * (size_t)g.blocks;
+}
+
+cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
+                            int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
+                            int32_t *hist, const DevStatus &ds, cudaStream_t st) {
+    const int64_t P = s.P();
+    const DispatchGrid g = dispatch_grid(P);
+    chunk_histogram_kernel<<<g.blocks, kThreads, sizeof(int) * s.E, st>>>(idx, P, s.E, g.chunk,
+                                                                        g.blocks, hist, ds);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    scan_kernel<<<1, kScanThreads, 0, st>>>(hist, s.E, g.blocks, counts, offsets);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const size_t sh = sizeof(int) * (size_t)kWarps * s.E;
+    scatter_kernel<<<g.blocks, kThreads, sh, st>>>(idx, P, s.k, s.E, g.chunk, g.blocks, hist, pos,
+                                                  src_token);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    const int row_vecs = (int)((int64_t)s.d * (s.bf16 ? 2 : 4) / 16);
+    const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
+    gather_rows_kernel<<<blocks, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), pos, P, s.k,
+                                                   row_vecs, static_cast<uint8_t *>(x_perm));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,616 @@
+// gemm_tc.cu -- grouped SwiGLU experts for bf16 activations on the sm_103a
+// tensor cores (tcgen05.mma, accumulators in tensor memory, operands staged
+// by TMA).
+//
+// Transformers docs "Expert parallelism", section "Adding an implementation"
+// (experts_forward runs each expert on the rows sent to it), and "Tensor
+// parallelism for inference", section "Packed strategies" (gate_up_proj is
+// [E][d][2f], applied as x @ gate_up_proj and split into gate = first f
+// columns, up = last f columns).  Two launches of one persistent kernel:
+//   G1: h_perm[r] = silu(x_perm[r] @ Wgu[e][:, :f]) * (x_perm[r] @ Wgu[e][:, f:])
+//   G2: y_perm[r] = h_perm[r] @ Wd[e]
+// for every expert e and row r of its segment [offsets[e], offsets[e+1]).
+//
+// Tiling.  A CTA tile is 128 rows x 256 accumulator columns; K advances 64
+// elements (128 bytes) per pipeline stage.  In G1 the 256 columns are 128
+// gate columns and the 128 matching up columns, so the SwiGLU is applied in
+// the epilogue straight from the two halves of one accumulator.  A (the
+// permuted activations) is K-major; B (the weights as stored, [K][N] with N
+// contiguous) is read MN-major, so no weight repacking is needed.
+//
+// Work list.  Row tiles never straddle experts: expert e owns
+// ceil(count_e / 128) row tiles and each CTA derives the prefix of those
+// counts from `offsets` on the device (no host synchronisation).  Tiles are
+// ordered expert-major, then column tile, then row tile, so CTAs running at
+// the same time share the same weight tile through L2.  The grid is
+// persistent (one CTA per SM) and strides over the tile list.
+//
+// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns the tensor
+// memory and issues the MMAs, warps 2-5 run the epilogue (tensor memory ->
+// registers -> global), each on its 32-lane quarter of the accumulator.  Two
+// accumulators (2 x 256 columns) let the epilogue of one tile overlap the
+// main loop of the next.
+//
+// Every wait is bounded (globaltimer); a wait that runs out records a timeout
+// in the device error word, raises a CTA-wide abort flag, and every role
+// drains its in-flight copies/MMAs before the tensor memory is released.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;          // accumulator columns per tile (MMA N)
+constexpr int BK = 64;           // K elements per stage = one 128-byte swizzle span
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit operands
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_ATOM_BYTES = BK * 128;        // 64 K-rows x 64 columns (128 B) = 8 KB
+constexpr int B_BYTES = 4 * B_ATOM_BYTES;     // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 2 * BN;             // two accumulators
+constexpr int NUM_THREADS = 192;
+constexpr int MAX_E = 1024;
+
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr int OFF_A = 0;
+constexpr int OFF_B = STAGES * A_BYTES;
+constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem_full, tmem_empty, drain
+constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_ABORT = OFF_TMEM + 4;
+constexpr int OFF_OFFS = OFF_ABORT + 4;                // int[MAX_E + 1]
+constexpr int OFF_TILE = OFF_OFFS + 4 * (MAX_E + 1);   // int[MAX_E + 1]
+constexpr int SMEM_USED = OFF_TILE + 4 * (MAX_E + 1);
+constexpr int SMEM_BYTES = SMEM_USED + 1024;           // slack for the 1024-byte alignment
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
+// A K-major, B MN-major, M = 128, N = 256.
+constexpr uint32_t IDESC = (1u << 4)            // D format: f32
+                           | (1u << 7)          // A format: bf16
+                           | (1u << 10)         // B format: bf16
+                           | (0u << 15)         // A major: K
+                           | (1u << 16)         // B major: MN
+                           | ((uint32_t)(BN >> 3) << 17)
+                           | ((uint32_t)(BM >> 4) << 24);
+
+struct Params {
+    const int32_t *offsets;
+    int E;
+    int K;        // reduction length (d for G1, f for G2)
+    int n_out;    // output columns (f for G1, d for G2)
+    int f;        // column offset of the up half in Wgu (G1)
+    int n_tiles;  // column tiles per row tile
+    __nv_bfloat16 *out;  // [P][n_out]
+    DevStatus ds;
+};
+
+// ----------------------------- PTX wrappers --------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns: thread i gets lane (base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (16-byte units), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;  // swizzle: 128 B
+    return d;
+}
+
+// Bounded wait: true when the phase with `parity` has completed; false when
+// the limit ran out or another role raised the abort flag.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
+                                             volatile int *abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > ds.wait_limit_ns) {
+            raise_error(ds, kErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+struct TileInfo {
+    int e, row0, rows, n_blk;
+};
+
+// Last e with s_tile[e] <= g, i.e. the expert whose row tiles hold g.
+__device__ __forceinline__ TileInfo decode_tile(int tile, const int *s_off, const int *s_tile,
+                                                int E, int n_tiles) {
+    const int g = tile / n_tiles;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (s_tile[mid] <= g) lo = mid; else hi = mid - 1;
+    }
+    TileInfo ti;
+    ti.e = lo;
+    const int mt = s_tile[lo + 1] - s_tile[lo];
+    const int r = tile - s_tile[lo] * n_tiles;
+    ti.n_blk = r / mt;
+    ti.row0 = s_off[lo] + (r % mt) * BM;
+    ti.rows = min(BM, s_off[lo + 1] - ti.row0);
+    return ti;
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+
+    const uint32_t bar_full = base_s + OFF_BAR;            // [STAGES]
+    const uint32_t bar_empty = bar_full + 8 * STAGES;      // [STAGES]
+    const uint32_t bar_tfull = bar_empty + 8 * STAGES;     // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;            // [2]
+    const uint32_t bar_drain = bar_tempty + 16;
+    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(base + OFF_ABORT);
+    int *s_off = reinterpret_cast<int *>(base + OFF_OFFS);
+    int *s_tile = reinterpret_cast<int *>(base + OFF_TILE);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+
+    // ---- prologue: row-tile prefix, barriers, tensor memory ----
+    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = p.offsets[e];
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_tfull + 8 * i, 1);
+            mbar_init(bar_tempty + 8 * i, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(bar_drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        tmem_alloc(base_s + OFF_TMEM, TMEM_COLS);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    if (warp == 2) {  // prefix of ceil(count_e / BM) over experts
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int local = 0;
+        for (int e = e0; e < e1; ++e) local += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+        int incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int run = incl - local;
+        for (int e = e0; e < e1; ++e) {
+            s_tile[e] = run;
+            run += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+        }
+        if (lane == 31) s_tile[E] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = *s_tmem;
+    const int n_tiles = p.n_tiles;
+    const int total = s_tile[E] * n_tiles;
+    const int nk = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        // ------------------------- TMA producer -------------------------
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t issued = 0, last_par = 0;  // per stage: ever issued, parity of last issue
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles);
+            const int n0 = ti.n_blk * (SWIGLU ? BN / 2 : BN);
+            for (int ks = 0; ks < nk; ++ks) {
+                int good = 1;
+                if (lane == 0) good = wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = bar_full + 8 * s;
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    const int k0 = ks * BK;
+                    tma_load_2d(base_s + OFF_A + s * A_BYTES, &tmA, k0, ti.row0, fb);
+                    const uint32_t bdst = base_s + OFF_B + s * B_BYTES;
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        int col;
+                        if (SWIGLU)
+                            col = (a < 2) ? (n0 + 64 * a) : (p.f + n0 + 64 * (a - 2));
+                        else
+                            col = n0 + 64 * a;
+                        tma_load_3d(bdst + a * B_ATOM_BYTES, &tmB, col, k0, ti.e, fb);
+                    }
+                    issued |= 1u << s;
+                    last_par = (last_par & ~(1u << s)) | (ph << s);
+                }
+                __syncwarp();
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        // drain: every issued load must have landed before the CTA exits
+        if (lane == 0) {
+            for (int i = 0; i < STAGES; ++i)
+                if ((issued >> i) & 1u) {
+                    volatile int never = 0;
+                    if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never)) break;
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------- MMA issuer ---------------------------
+        int s = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            int good = 1;
+            if (lane == 0) good = wait_bounded(bar_tempty + 8 * acc, aph ^ 1u, p.ds, s_abort);
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int ks = 0; ks < nk; ++ks) {
+                good = 1;
+                if (lane == 0) good = wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort);
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t a_s = base_s + OFF_A + s * A_BYTES;
+                    const uint32_t b_s = base_s + OFF_B + s * B_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
+                        //    K step of 16 elements = 32 bytes along the row.
+                        const uint64_t adesc = smem_desc_sw128(a_s + kk * 32, 16, 1024);
+                        // B: MN-major, 64-column atoms 8 KB apart (LBO), 8-row K
+                        //    groups 1024 B apart (SBO); K step of 16 rows = 2 KB.
+                        const uint64_t bdesc = smem_desc_sw128(b_s + kk * 2048, B_ATOM_BYTES, 1024);
+                        mma_bf16(d_tmem, adesc, bdesc, (ks | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_empty + 8 * s);  // frees the stage once these MMAs finish
+                }
+                __syncwarp();
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(bar_tfull + 8 * acc);  // accumulator ready
+            __syncwarp();
+        }
+        // drain: all MMAs issued by this thread complete before tensor memory is freed
+        if (lane == 0) {
+            mma_commit(bar_drain);
+            volatile int never = 0;
+            wait_bounded(bar_drain, 0, p.ds, &never);
+        }
+        __syncwarp();
+    } else {
+        // --------------------------- epilogue ----------------------------
+        const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
+        const int r_in_tile = quarter * 32 + lane;
+        int it = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles);
+            const int acc = it & 1;
+            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+            const int good = __all_sync(0xffffffffu,
+                                        wait_bounded(bar_tfull + 8 * acc, aph, p.ds, s_abort));
+            if (!good) break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
+            const bool row_ok = r_in_tile < ti.rows;
+            __nv_bfloat16 *orow = p.out + (int64_t)(ti.row0 + r_in_tile) * p.n_out;
+            if (SWIGLU) {
+                const int n0 = ti.n_blk * (BN / 2);
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(t_row + c, g);
+                    tmem_ld32(t_row + BN / 2 + c, u);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                        float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                        float h0 = g0 / (1.f + __expf(-g0)) * u0;
+                        float h1 = g1 / (1.f + __expf(-g1)) * u1;
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
+                        packed[i] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = n0 + c + 8 * v;
+                            if (col + 8 <= p.n_out)
+                                stg16(orow + col, make_uint4(packed[4 * v], packed[4 * v + 1],
+                                                             packed[4 * v + 2], packed[4 * v + 3]));
+                        }
+                    }
+                }
+            } else {
+                const int n0 = ti.n_blk * BN;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t y[32];
+                    tmem_ld32(t_row + c, y);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(y[2 * i]),
+                                                                  __uint_as_float(y[2 * i + 1]));
+                        packed[i] = *reinterpret_cast<uint32_t *>(&b2);
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = n0 + c + 8 * v;
+                            if (col + 8 <= p.n_out)
+                                stg16(orow + col, make_uint4(packed[4 * v], packed[4 * v + 1],
+                                                             packed[4 * v + 2], packed[4 * v + 3]));
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------ host side ----------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// Rows x cols bf16 matrix (cols contiguous), box 64 cols x 128 rows, 128 B swizzle.
+bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// E x K x N bf16 weights (N contiguous), box 64 cols x 64 K-rows x 1 expert.
+bool make_map_weights(CUtensorMap *m, const void *ptr, int64_t E, int64_t K, int64_t N) {
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)E};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)BK, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
+                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+};
+
+}  // namespace tc
+
+cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
+                                     const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
+                                     const DevStatus &ds, cudaStream_t st) {
+    using namespace tc;
+    static DeviceInfo info[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!info[dev].ready) {
+        if ((err = cudaDeviceGetAttribute(&info[dev].sms, cudaDevAttrMultiProcessorCount, dev)) !=
+            cudaSuccess)
+            return err;
+        if ((err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES)) != cudaSuccess)
+            return err;
+        if ((err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        SMEM_BYTES)) != cudaSuccess)
+            return err;
+        info[dev].ready = true;
+    }
+    if (!encode_fn()) {
+        set_error_message("cuTensorMapEncodeTiled is not available from the driver");
+        return cudaErrorNotSupported;
+    }
+    const int64_t P = s.P();
+    CUtensorMap mx, mwgu, mh, mwd;
+    if (!make_map_rows(&mx, x_perm, P, s.d) || !make_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) ||
+        !make_map_rows(&mh, h_perm, P, s.f) || !make_map_weights(&mwd, Wd, s.E, s.f, s.d)) {
+        set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
+        return cudaErrorInvalidValue;
+    }
+    // Upper bound of the row tiles (sum_e ceil(count_e/BM) <= P/BM + E) times the column tiles.
+    const int64_t row_tiles_max = (P + BM - 1) / BM + std::min<int64_t>(s.E, P);
+
+    Params p1;
+    p1.offsets = offsets;
+    p1.E = s.E;
+    p1.K = s.d;
+    p1.n_out = s.f;
+    p1.f = s.f;
+    p1.n_tiles = (s.f + BN / 2 - 1) / (BN / 2);
+    p1.out = static_cast<__nv_bfloat16 *>(h_perm);
+    p1.ds = ds;
+    int64_t bound1 = row_tiles_max * p1.n_tiles;
+    if (bound1 >= (int64_t)INT32_MAX || row_tiles_max * ((s.d + BN - 1) / BN) >= (int64_t)INT32_MAX) {
+        set_error_message("grouped GEMM tile count exceeds 2^31");
+        return cudaErrorInvalidValue;
+    }
+    unsigned grid1 = (unsigned)std::min<int64_t>(info[dev].sms, bound1);
+    grouped_gemm_tc_kernel<true><<<grid1, NUM_THREADS, SMEM_BYTES, st>>>(mx, mwgu, p1);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+    Params p2 = p1;
+    p2.K = s.f;
+    p2.n_out = s.d;
+    p2.f = 0;
+    p2.n_tiles = (s.d + BN - 1) / BN;
+    p2.out = static_cast<__nv_bfloat16 *>(y_perm);
+    int64_t bound2 = row_tiles_max * p2.n_tiles;
+    unsigned grid2 = (unsigned)std::min<int64_t>(info[dev].sms, bound2);
+    grouped_gemm_tc_kernel<false><<<grid2, NUM_THREADS, SMEM_BYTES, st>>>(mh, mwd, p2);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,53 @@
+// kernels.h -- host-side launchers of the libmoe kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct Shape {
+    int64_t T;
+    int d, E, k, f;
+    bool bf16;    // activation dtype: bf16 (else fp32)
+    bool renorm;  // renormalise the chosen k weights
+    int64_t P() const { return T * (int64_t)k; }
+};
+
+// Router: logits[T][E] = x @ Wr^T (+ bias), fp32 accumulation.
+cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr,
+                                 const float *bias, float *logits, cudaStream_t st);
+// Top-k selection and softmax weights on a given fp32 logit buffer.
+cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
+                        cudaStream_t st);
+
+// Dispatch: chunking of the P pairs over histogram/scatter blocks.
+struct DispatchGrid {
+    int chunk;  // pairs per block (multiple of 256)
+    int blocks;  // number of blocks (>= 1 when P > 0)
+};
+DispatchGrid dispatch_grid(int64_t P);
+size_t dispatch_scratch_bytes(const Shape &s);  // per-block histogram ints
+cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
+                            int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
+                            int32_t *hist, const DevStatus &ds, cudaStream_t st);
+
+// Grouped SwiGLU experts.  bf16: tcgen05 tensor-core path; fp32: SIMT path.
+cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
+                                     const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
+                                     const DevStatus &ds, cudaStream_t st);
+cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const int32_t *offsets,
+                                      const float *Wgu, const float *Wd, float *h_perm,
+                                      float *y_perm, cudaStream_t st);
+
+// Weighted combine of the expert rows back into token order.
+cudaError_t launch_combine(const Shape &s, const void *y_perm, const int32_t *pos, const float *w,
+                           void *out, cudaStream_t st);
+
+// Last detailed message set by a launcher (thread-local; empty if none).
+void set_error_message(const char *fmt, ...);
+const char *error_message();
+
+}  // namespace moe
