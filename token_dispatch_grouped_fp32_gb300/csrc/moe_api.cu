@@ -133,7 +133,7 @@ moe_status_t check_ptrs(std::initializer_list<const void *> ptrs) {
 
 moe_status_t from_cuda(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return MOE_OK;
-    if (error_message()[0] == 0 || strstr(error_message(), what) == nullptr)
+    if (error_message()[0] == 0)  // keep a launcher's more specific message
         set_error_message("%s: %s", what, cudaGetErrorString(e));
     return MOE_ERR_CUDA;
 }
@@ -227,12 +227,12 @@ moe_status_t moe_route(const moe_config_t *cfg, const void *x, const float *Wr,
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({x, Wr, logits, topk_idx, topk_w})) != MOE_OK) return st;
     if (logit_bias && !aligned16(logit_bias)) {
         set_error_message("logit_bias is not 16-byte aligned");
         return MOE_ERR_INVALID_ARG;
     }
-    if (s.T == 0) return MOE_OK;
     DevStatus ds;
     if ((st = device_status(&ds)) != MOE_OK) return st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -247,8 +247,8 @@ moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits,
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({logits, topk_idx, topk_w})) != MOE_OK) return st;
-    if (s.T == 0) return MOE_OK;
     DevStatus ds;
     if ((st = device_status(&ds)) != MOE_OK) return st;
     return from_cuda(launch_topk(s, logits, topk_idx, topk_w, static_cast<cudaStream_t>(stream)),
@@ -262,9 +262,9 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, cons
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({topk_idx, x, counts, offsets, pos, src_token, x_perm, ws})) != MOE_OK)
         return st;
-    if (s.T == 0) return MOE_OK;
     if (ws_bytes < dispatch_scratch_bytes(s)) {
         set_error_message("workspace %zu bytes < %zu needed", ws_bytes, dispatch_scratch_bytes(s));
         return MOE_ERR_WORKSPACE;
@@ -284,9 +284,9 @@ moe_status_t moe_grouped_swiglu(const moe_config_t *cfg, const void *x_perm,
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({x_perm, offsets, W_gate_up, W_down, h_perm, y_perm})) != MOE_OK)
         return st;
-    if (s.T == 0) return MOE_OK;
     DevStatus ds;
     if ((st = device_status(&ds)) != MOE_OK) return st;
     return run_experts(s, x_perm, offsets, W_gate_up, W_down, h_perm, y_perm, ds,
@@ -299,8 +299,8 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int3
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({y_perm, pos, topk_w, out})) != MOE_OK) return st;
-    if (s.T == 0) return MOE_OK;
     DevStatus ds;
     if ((st = device_status(&ds)) != MOE_OK) return st;
     return from_cuda(launch_combine(s, y_perm, pos, topk_w, out, static_cast<cudaStream_t>(stream)),
@@ -314,12 +314,12 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({x, Wr, W_gate_up, W_down, out, ws})) != MOE_OK) return st;
     if (logit_bias && !aligned16(logit_bias)) {
         set_error_message("logit_bias is not 16-byte aligned");
         return MOE_ERR_INVALID_ARG;
     }
-    if (s.T == 0) return MOE_OK;
     const WsLayout L = ws_layout(s);
     if (ws_bytes < L.total) {
         set_error_message("workspace %zu bytes < %zu needed", ws_bytes, L.total);
@@ -356,8 +356,8 @@ moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_host, const
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({x_host, out_host, x_dev, out_dev})) != MOE_OK) return st;
-    if (s.T == 0) return MOE_OK;
     const size_t bytes = (size_t)s.T * s.d * (s.bf16 ? 2 : 4);
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if ((st = from_cuda(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, cs),
