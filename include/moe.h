@@ -141,6 +141,33 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
                           void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * moe_dispatch without a caller workspace.  (The pages have no counterpart:
+ * this is a deployment variant of the same dispatch.)
+ *
+ * For callers that cannot allocate device memory for scratch: a plugin whose
+ * host framework owns all device memory and passes only the layer's inputs
+ * and outputs, or a service that must not call cudaMalloc after start-up.
+ * The histogram scratch moe_dispatch would take from `ws` lives instead in a
+ * fixed 1 MiB array inside the library (262,144 int32 entries, held on every
+ * GPU that loads the library until the process exits).  Results are
+ * identical to moe_dispatch.  This call allocates nothing and calls no
+ * allocating routine.
+ *
+ * Limit: moe_dispatch_workspace_size(cfg) must be <= 1 MiB (E times the
+ * number of 2048-pair chunks <= 262,144: any P for E <= 256; P <= 524,288
+ * for E = 1024); larger sizes return MOE_ERR_UNSUPPORTED and launch nothing.
+ * Set-up: the first call with T > 0 on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current, once; make that
+ * first call before any stream capture.  All calls on a device share the
+ * array, so calls whose kernels overlap on the GPU race: serialise them.
+ * Other arguments, errors and outputs are as for moe_dispatch.
+ */
+moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int32_t *topk_idx,
+                                  const void *x, int32_t *counts, int32_t *offsets,
+                                  int32_t *pos, int32_t *src_token, void *x_perm,
+                                  void *stream);
+
+/*
  * Grouped SwiGLU experts [EP-add: experts_forward; TP-pack]: for every expert
  * e and every row r in [offsets[e], offsets[e+1]):
  *   gu        = x_perm[r] @ W_gate_up[e]        (W_gate_up: [E][d][2f])
