@@ -14,12 +14,129 @@ namespace moe {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Router logits: C[T][E] = A[T][d] * B[E][d]^T (+ bias[E]), fp32 FFMA.
-// Block tile BM x BN, K step BK; each thread owns TM x TN outputs spread with
-// stride (BM/TM) rows and (BN/TN) columns so shared-memory reads are
-// conflict-free.  Operand tiles are stored k-major with one word of padding.
+// Router logits, warp-split form (used for E <= 32, and for larger E when the
+// batch is small).  A block owns TPW tokens x EP experts (TPW * EP = 32;
+// EP = E rounded up to a power of two, or 32-expert groups along blockIdx.y
+// when E > 32).  Its 8 warps split the hidden dimension: warp w, lane l
+// walks 8-element chunks q = 32w + l, q + 256, ... with 16-byte loads of x
+// and two float4 loads per expert of Wr, keeping 32 partial sums.  A
+// butterfly reduce-scatter (31 shuffles) leaves partial i of every warp in
+// lane i; warp 0 then adds the 8 warps' values in warp order (a fixed order,
+// so results are reproducible) and lane i writes logit (token i/EP, expert
+// e0 + i%EP).
 // ---------------------------------------------------------------------------
-constexpr int kLogitBK = 32;
+template <typename TA> struct Chunk8;
+template <> struct Chunk8<__nv_bfloat16> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&v)[8]) {
+        unpack16(ldg16(p), v, static_cast<const __nv_bfloat16 *>(nullptr));
+    }
+};
+template <> struct Chunk8<float> {
+    static __device__ __forceinline__ void load(const float *p, float (&v)[8]) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
+// After the call lane l holds the warp-wide sum of v[l] in v[0].
+__device__ __forceinline__ void warp_reduce_scatter32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int half = 16; half >= 1; half >>= 1) {
+        const bool upper = (lane & half) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+            const float send = upper ? v[j] : v[j + half];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, half);
+            v[j] = (upper ? v[j + half] : v[j]) + recv;
+        }
+    }
+}
+
+constexpr int kSplitWarps = 8;
+
+template <typename TA, int EP>
+__global__ void __launch_bounds__(256)
+router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
+                           const float *__restrict__ bias, float *__restrict__ logits,
+                           int64_t T, int d, int E) {
+    constexpr int TPW = 32 / EP;
+    __shared__ float red[kSplitWarps][32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * TPW;
+    const int e0 = blockIdx.y * EP;
+    const int ne = min(EP, E - e0);  // experts of this block's group
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    const TA *xr[TPW];
+#pragma unroll
+    for (int tt = 0; tt < TPW; ++tt) xr[tt] = x + min(t0 + tt, T - 1) * d;
+    const float *wr = Wr + (int64_t)e0 * d;
+    for (int c = (wid * 32 + lane) * 8; c < d; c += 32 * kSplitWarps * 8) {
+        if constexpr (EP > TPW) {
+            // hold the TPW token chunks, stream the experts
+            float xv[TPW][8];
+#pragma unroll
+            for (int tt = 0; tt < TPW; ++tt) Chunk8<TA>::load(xr[tt] + c, xv[tt]);
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                if (e < ne) {
+                    float wv[8];
+                    Chunk8<float>::load(wr + (int64_t)e * d + c, wv);
+#pragma unroll
+                    for (int tt = 0; tt < TPW; ++tt)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc[tt * EP + e] = fmaf(xv[tt][i], wv[i], acc[tt * EP + e]);
+                }
+            }
+        } else {
+            // hold the EP expert chunks, stream the tokens
+            float wv[EP][8];
+#pragma unroll
+            for (int e = 0; e < EP; ++e) {
+                if (e < ne) Chunk8<float>::load(wr + (int64_t)e * d + c, wv[e]);
+                else
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) wv[e][i] = 0.f;
+            }
+#pragma unroll
+            for (int tt = 0; tt < TPW; ++tt) {
+                float xv[8];
+                Chunk8<TA>::load(xr[tt] + c, xv);
+#pragma unroll
+                for (int e = 0; e < EP; ++e)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[tt * EP + e] = fmaf(xv[i], wv[e][i], acc[tt * EP + e]);
+            }
+        }
+    }
+    warp_reduce_scatter32(acc);
+    red[wid][lane] = acc[0];
+    __syncthreads();
+    if (wid == 0) {
+        float v = red[0][lane];
+#pragma unroll
+        for (int w = 1; w < kSplitWarps; ++w) v += red[w][lane];
+        const int tt = lane / EP, e = lane % EP;
+        const int64_t t = t0 + tt;
+        if (e < ne && t < T) logits[t * E + e0 + e] = v + (bias ? bias[e0 + e] : 0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Router logits, larger E: C[T][E] = A[T][d] * B[E][d]^T (+ bias[E]), fp32
+// FFMA.  Block tile BM x BN, K step BK; each thread owns TM x TN outputs
+// spread with stride (BM/TM) rows and (BN/TN) columns so shared-memory reads
+// are conflict-free.  Operand tiles are stored k-major with one word of
+// padding and double-buffered: the next K step is fetched into registers
+// while the current one is multiplied.
+// ---------------------------------------------------------------------------
+constexpr int kLogitBK = 16;
 
 template <typename TA, int BM, int BN, int TM, int TN>
 __global__ void __launch_bounds__(256)
@@ -30,8 +147,9 @@ router_logits_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
     constexpr int BK = kLogitBK;
     constexpr int RG = BM / TM;  // row groups
     constexpr int CG = BN / TN;  // column groups
-    __shared__ float As[BK][BM + 1];
-    __shared__ float Bs[BK][BN + 1];
+    constexpr int AL = BM * BK / 256, BL = BN * BK / 256;  // loads per thread
+    __shared__ float As[2][BK][BM + 1];
+    __shared__ float Bs[2][BK][BN + 1];
 
     const int tid = threadIdx.x;
     const int tx = tid % CG, ty = tid / CG;
@@ -44,35 +162,55 @@ router_logits_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
 #pragma unroll
         for (int j = 0; j < TN; ++j) acc[i][j] = 0.f;
 
-    for (int k0 = 0; k0 < d; k0 += BK) {
-        for (int i = tid; i < BM * BK; i += 256) {
-            int r = i / BK, c = i % BK;
-            int64_t gm = m0 + r;
-            int gk = k0 + c;
-            float v = 0.f;
-            if (gm < T && gk < d) v = Act<TA>::to_f(x[gm * d + gk]);
-            As[c][r] = v;
+    float ra[AL], rb[BL];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int l = 0; l < AL; ++l) {
+            const int i = tid + l * 256, r = i / BK, c = i % BK;
+            const int64_t gm = m0 + r;
+            const int gk = k0 + c;
+            ra[l] = (gm < T && gk < d) ? Act<TA>::to_f(x[gm * d + gk]) : 0.f;
         }
-        for (int i = tid; i < BN * BK; i += 256) {
-            int r = i / BK, c = i % BK;
-            int gn = n0 + r, gk = k0 + c;
-            float v = 0.f;
-            if (gn < E && gk < d) v = Wr[(int64_t)gn * d + gk];
-            Bs[c][r] = v;
+#pragma unroll
+        for (int l = 0; l < BL; ++l) {
+            const int i = tid + l * 256, r = i / BK, c = i % BK;
+            const int gn = n0 + r, gk = k0 + c;
+            rb[l] = (gn < E && gk < d) ? Wr[(int64_t)gn * d + gk] : 0.f;
         }
-        __syncthreads();
-#pragma unroll 8
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+        for (int l = 0; l < AL; ++l) {
+            const int i = tid + l * 256;
+            As[buf][i % BK][i / BK] = ra[l];
+        }
+#pragma unroll
+        for (int l = 0; l < BL; ++l) {
+            const int i = tid + l * 256;
+            Bs[buf][i % BK][i / BK] = rb[l];
+        }
+    };
+
+    const int nk = (d + BK - 1) / BK;
+    fetch(0);
+    stash(0);
+    __syncthreads();
+    for (int kt = 0; kt < nk; ++kt) {
+        const int buf = kt & 1;
+        if (kt + 1 < nk) fetch((kt + 1) * BK);
+#pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             float a[TM], b[TN];
 #pragma unroll
-            for (int i = 0; i < TM; ++i) a[i] = As[kk][ty + i * RG];
+            for (int i = 0; i < TM; ++i) a[i] = As[buf][kk][ty + i * RG];
 #pragma unroll
-            for (int j = 0; j < TN; ++j) b[j] = Bs[kk][tx + j * CG];
+            for (int j = 0; j < TN; ++j) b[j] = Bs[buf][kk][tx + j * CG];
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
+        if (kt + 1 < nk) stash(buf ^ 1);
         __syncthreads();
     }
 #pragma unroll
@@ -95,12 +233,27 @@ cudaError_t launch_logits_cfg(const Shape &s, const TA *x, const float *Wr, cons
     return cudaGetLastError();
 }
 
+template <typename TA, int EP>
+cudaError_t launch_logits_split(const Shape &s, const TA *x, const float *Wr, const float *bias,
+                                float *logits, cudaStream_t st) {
+    constexpr int TPW = 32 / EP;
+    dim3 grid((unsigned)((s.T + TPW - 1) / TPW), (unsigned)((s.E + EP - 1) / EP));
+    router_logits_split_kernel<TA, EP><<<grid, 256, 0, st>>>(x, Wr, bias, logits, s.T, s.d, s.E);
+    return cudaGetLastError();
+}
+
 template <typename TA>
 cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const float *bias,
                             float *logits, cudaStream_t st) {
-    if (s.E <= 8) return launch_logits_cfg<TA, 64, 8, 2, 1>(s, x, Wr, bias, logits, st);
-    if (s.E <= 16) return launch_logits_cfg<TA, 64, 16, 4, 1>(s, x, Wr, bias, logits, st);
-    if (s.E <= 32) return launch_logits_cfg<TA, 64, 32, 4, 2>(s, x, Wr, bias, logits, st);
+    if (s.E <= 1) return launch_logits_split<TA, 1>(s, x, Wr, bias, logits, st);
+    if (s.E <= 2) return launch_logits_split<TA, 2>(s, x, Wr, bias, logits, st);
+    if (s.E <= 4) return launch_logits_split<TA, 4>(s, x, Wr, bias, logits, st);
+    if (s.E <= 8) return launch_logits_split<TA, 8>(s, x, Wr, bias, logits, st);
+    if (s.E <= 16) return launch_logits_split<TA, 16>(s, x, Wr, bias, logits, st);
+    if (s.E <= 32) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, st);
+    // larger E: the tiled kernel re-reads Wr far less per token, but needs
+    // enough row tiles to fill the GPU; small batches use 32-expert groups.
+    if (s.T < 2048) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, st);
     if (s.E <= 64) return launch_logits_cfg<TA, 64, 64, 4, 4>(s, x, Wr, bias, logits, st);
     return launch_logits_cfg<TA, 64, 128, 4, 8>(s, x, Wr, bias, logits, st);
 }
