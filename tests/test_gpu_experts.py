@@ -1,6 +1,8 @@
 """Grouped SwiGLU parity: h_perm and y_perm of every row against the oracle's
 expert FFN, for ragged segments (empty experts, partial row tiles, partial
-column tiles and a partial K step)."""
+column tiles and a partial K step), with both tile shapes: 128-row tiles on
+one CTA (small per-expert batches) and 256-row tiles on a CTA pair (batches
+averaging >= 512 rows per expert)."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +25,10 @@ EXPERT_CASES = [
     ([513], 64, 1024),                  # one expert, 5 row tiles
     ([40] * 16, 320, 136),
     ([0, 0, 0, 9], 72, 8),              # tiny f: one partial column vector
+    # >= 512 rows per expert on average: CTA-pair tiles (256 rows)
+    ([0, 700, 1030, 5, 1500], 264, 200),
+    ([600, 0, 900], 128, 384),
+    ([2049], 64, 136),
 ]
 
 

@@ -11,25 +11,39 @@
 //   G2: y_perm[r] = h_perm[r] @ Wd[e]
 // for every expert e and row r of its segment [offsets[e], offsets[e+1]).
 //
-// Tiling.  A CTA tile is 128 rows x 256 accumulator columns; K advances 64
-// elements (128 bytes) per pipeline stage.  In G1 the 256 columns are 128
-// gate columns and the 128 matching up columns, so the SwiGLU is applied in
-// the epilogue straight from the two halves of one accumulator.  A (the
-// permuted activations) is K-major; B (the weights as stored, [K][N] with N
-// contiguous) is read MN-major, so no weight repacking is needed.
+// Tiling.  Two tile shapes share one kernel template (CTAS = 1 or 2).
+//  - CTAS = 2 (a cluster of 2, tcgen05.mma.cta_group::2): the pair owns a
+//    256-row x 256-column tile; each CTA holds its 128 rows of A and half of
+//    the 256 B columns in its own shared memory, and the leader CTA's MMA
+//    (M = 256, N = 256, K = 16) reads both halves and writes each CTA's 128
+//    rows into that CTA's tensor memory.  Per K step a CTA loads 16 KB of A
+//    and 16 KB of B, so six stages fit; used when experts receive many rows.
+//  - CTAS = 1 (tcgen05.mma.cta_group::1): a CTA owns a 128 x 256 tile and
+//    loads 16 KB of A and 32 KB of B per K step (four stages).  Row tiles of
+//    128 waste less on ragged segments, so it serves small per-expert batches
+//    (decode, or ~256 rows per expert), where the weight stream bounds.
+// A K step is 64 elements (128 bytes: one swizzle span).  In G1 the 256
+// accumulator columns are 128 gate columns and the 128 matching up columns,
+// so the SwiGLU is applied in the epilogue straight from the two halves of
+// one accumulator.  A (the permuted activations) is K-major; B (the weights
+// as stored, [K][N] with N contiguous) is read MN-major, so no weight
+// repacking is needed.
 //
 // Work list.  Row tiles never straddle experts: expert e owns
-// ceil(count_e / 128) row tiles and each CTA derives the prefix of those
-// counts from `offsets` on the device (no host synchronisation).  Tiles are
-// ordered expert-major, then column tile, then row tile, so CTAs running at
-// the same time share the same weight tile through L2.  The grid is
-// persistent (one CTA per SM) and strides over the tile list.
+// ceil(count_e / tile rows) row tiles and each CTA derives the prefix of
+// those counts from `offsets` on the device (no host synchronisation).
+// Tiles are ordered expert-major, then column tile, then row tile, so tiles
+// running at the same time share the same weight tile through L2.  The grid
+// is persistent (as many CTAs or pairs as fit at once) and strides over the
+// tile list.
 //
-// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns the tensor
-// memory and issues the MMAs, warps 2-5 run the epilogue (tensor memory ->
-// registers -> global), each on its 32-lane quarter of the accumulator.  Two
-// accumulators (2 x 256 columns) let the epilogue of one tile overlap the
-// main loop of the next.
+// Roles (192 threads per CTA): warp 0 issues TMA loads, warp 1 owns the
+// tensor memory and issues the MMAs and their commits (in a pair: the leader
+// only, commits multicast to both CTAs, and every load of both CTAs signals
+// the leader's full barrier), warps 2-5 run the epilogue (tensor memory ->
+// registers -> global), each on its 32-lane quarter of its CTA's
+// accumulator.  Two accumulators (2 x 256 columns) let the epilogue of one
+// tile overlap the main loop of the next.
 //
 // Every wait is bounded (globaltimer); a wait that runs out records a timeout
 // in the device error word, raises a CTA-wide abort flag, and every role
@@ -44,40 +58,46 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128;
+constexpr int BM = 128;          // rows per CTA
 constexpr int BN = 256;          // accumulator columns per tile (MMA N)
 constexpr int BK = 64;           // K elements per stage = one 128-byte swizzle span
-constexpr int STAGES = 4;
 constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit operands
-constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
 constexpr int B_ATOM_BYTES = BK * 128;        // 64 K-rows x 64 columns (128 B) = 8 KB
-constexpr int B_BYTES = 4 * B_ATOM_BYTES;     // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 2 * BN;             // two accumulators
 constexpr int NUM_THREADS = 192;
 constexpr int MAX_E = 1024;
+constexpr int kPairRowsPerExpert = 512;  // average rows per expert that selects CTA pairs
 
-// Shared-memory map (offsets from a 1024-byte aligned base).
-constexpr int OFF_A = 0;
-constexpr int OFF_B = STAGES * A_BYTES;
-constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem_full, tmem_empty, drain
-constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
-constexpr int OFF_ABORT = OFF_TMEM + 4;
-constexpr int OFF_OFFS = OFF_ABORT + 4;                // int[MAX_E + 1]
-constexpr int OFF_TILE = OFF_OFFS + 4 * (MAX_E + 1);   // int[MAX_E + 1]
-constexpr int SMEM_USED = OFF_TILE + 4 * (MAX_E + 1);
-constexpr int SMEM_BYTES = SMEM_USED + 1024;           // slack for the 1024-byte alignment
-
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
-// A K-major, B MN-major, M = 128, N = 256.
-constexpr uint32_t IDESC = (1u << 4)            // D format: f32
-                           | (1u << 7)          // A format: bf16
-                           | (1u << 10)         // B format: bf16
-                           | (0u << 15)         // A major: K
-                           | (1u << 16)         // B major: MN
-                           | ((uint32_t)(BN >> 3) << 17)
-                           | ((uint32_t)(BM >> 4) << 24);
+template <int CTAS> struct Cfg {
+    static constexpr bool PAIR = CTAS == 2;
+    static constexpr int TILE_M = BM * CTAS;              // rows per tile (MMA M)
+    static constexpr int B_ATOMS = 4 / CTAS;              // 64-column B atoms per CTA
+    static constexpr int B_BYTES = B_ATOMS * B_ATOM_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int EXPECT_BYTES = STAGE_BYTES * CTAS;  // per full-barrier phase
+    // shared-memory map (offsets from a 1024-byte aligned base)
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = STAGES * A_BYTES;
+    static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem full/empty, drain
+    static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int OFF_OFFS = OFF_ABORT + 4;               // int[MAX_E + 1]
+    static constexpr int OFF_TILE = OFF_OFFS + 4 * (MAX_E + 1);  // int[MAX_E + 1]
+    static constexpr int SMEM_BYTES = OFF_TILE + 4 * (MAX_E + 1) + 1024;  // + alignment slack
+    // instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
+    // A K-major, B MN-major, M = TILE_M, N = 256
+    static constexpr uint32_t IDESC = (1u << 4)       // D format: f32
+                                      | (1u << 7)     // A format: bf16
+                                      | (1u << 10)    // B format: bf16
+                                      | (0u << 15)    // A major: K
+                                      | (1u << 16)    // B major: MN
+                                      | ((uint32_t)(BN >> 3) << 17)
+                                      | ((uint32_t)(TILE_M >> 4) << 24);
+    static constexpr int EPI_ARRIVALS = 4 * CTAS;         // epilogue warps reporting per tile
+};
 
 struct Params {
     const int32_t *offsets;
@@ -93,6 +113,21 @@ struct Params {
 // ----------------------------- PTX wrappers --------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -115,21 +150,45 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// Arrive on a barrier anywhere in the cluster (cluster-window address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+// TMA tile loads into this CTA's shared memory.  CTAS = 1: completion on a
+// barrier of this CTA.  CTAS = 2: on a barrier of either CTA of the pair
+// (cluster-window address).
+template <int CTAS>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
                                             uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
+    if constexpr (CTAS == 2)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
+            : "memory");
 }
+template <int CTAS>
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
                                             int c2, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
+    if constexpr (CTAS == 2)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+            : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -137,31 +196,76 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
+// Tensor-memory allocation: one warp of the CTA (CTAS = 1), or one warp of
+// each CTA of the pair together (CTAS = 2).
+template <int CTAS> __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    if constexpr (CTAS == 2) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dst_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         dst_smem),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
 }
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+template <int CTAS> __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    if constexpr (CTAS == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+                     "r"(ncols)
+                     : "memory");
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
+template <int CTAS>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
-        : "memory");
+    if constexpr (CTAS == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(Cfg<2>::IDESC), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(adesc), "l"(bdesc), "r"(Cfg<1>::IDESC), "r"(accumulate)
+            : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
+// Arrive on the barrier at offset `bar` (in both CTAs of a pair) once this
+// thread's earlier MMAs have completed.
+template <int CTAS> __device__ __forceinline__ void mma_commit_all(uint32_t bar) {
+    if constexpr (CTAS == 2) {
+        const uint16_t mask = 0x3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar), "h"(mask)
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    }
+}
+// ... on this CTA's barrier only.
+template <int CTAS> __device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+    if constexpr (CTAS == 2)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
 }
 // 32 lanes x 32 consecutive fp32 columns: thread i gets lane (base + i).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -214,12 +318,12 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
 }
 
 struct TileInfo {
-    int e, row0, rows, n_blk;
+    int e, row0, rows, n_blk;  // row0/rows: the tile's slice of expert e's segment
 };
 
 // Last e with s_tile[e] <= g, i.e. the expert whose row tiles hold g.
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int *s_off, const int *s_tile,
-                                                int E, int n_tiles) {
+                                                int E, int n_tiles, int tile_m) {
     const int g = tile / n_tiles;
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -231,32 +335,42 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *s_off, cons
     const int mt = s_tile[lo + 1] - s_tile[lo];
     const int r = tile - s_tile[lo] * n_tiles;
     ti.n_blk = r / mt;
-    ti.row0 = s_off[lo] + (r % mt) * BM;
-    ti.rows = min(BM, s_off[lo + 1] - ti.row0);
+    ti.row0 = s_off[lo] + (r % mt) * tile_m;
+    ti.rows = min(tile_m, s_off[lo + 1] - ti.row0);
     return ti;
 }
 
-template <bool SWIGLU>
+template <bool SWIGLU, int CTAS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, Params p) {
+    using C = Cfg<CTAS>;
+    constexpr bool PAIR = C::PAIR;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_s - raw_s);
 
-    const uint32_t bar_full = base_s + OFF_BAR;            // [STAGES]
+    const uint32_t bar_full = base_s + C::OFF_BAR;         // [STAGES] (a pair uses the leader's)
     const uint32_t bar_empty = bar_full + 8 * STAGES;      // [STAGES]
     const uint32_t bar_tfull = bar_empty + 8 * STAGES;     // [2]
-    const uint32_t bar_tempty = bar_tfull + 16;            // [2]
+    const uint32_t bar_tempty = bar_tfull + 16;            // [2] (a pair uses the leader's)
     const uint32_t bar_drain = bar_tempty + 16;
-    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + OFF_TMEM);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(base + OFF_ABORT);
-    int *s_off = reinterpret_cast<int *>(base + OFF_OFFS);
-    int *s_tile = reinterpret_cast<int *>(base + OFF_TILE);
+    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + C::OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(base + C::OFF_ABORT);
+    int *s_off = reinterpret_cast<int *>(base + C::OFF_OFFS);
+    int *s_tile = reinterpret_cast<int *>(base + C::OFF_TILE);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;  // 0: the CTA that issues the MMAs
+    const bool leader = rank == 0;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nunits = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    // barriers every load / epilogue signals (the leader's, in a pair)
+    const uint32_t sig_full = PAIR ? map_to_rank(bar_full, 0) : bar_full;
+    const uint32_t sig_tempty = PAIR ? map_to_rank(bar_tempty, 0) : bar_tempty;
 
     // ---- prologue: row-tile prefix, barriers, tensor memory ----
     for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = p.offsets[e];
@@ -268,22 +382,19 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_tfull + 8 * i, 1);
-            mbar_init(bar_tempty + 8 * i, 4);  // one arrival per epilogue warp
+            mbar_init(bar_tempty + 8 * i, C::EPI_ARRIVALS);
         }
         mbar_init(bar_drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 1) {
-        tmem_alloc(base_s + OFF_TMEM, TMEM_COLS);
-        tmem_relinquish();
-    }
+    if (warp == 1) tmem_alloc<CTAS>(base_s + C::OFF_TMEM, TMEM_COLS);
     __syncthreads();
-    if (warp == 2) {  // prefix of ceil(count_e / BM) over experts
+    if (warp == 2) {  // prefix of ceil(count_e / TILE_M) over experts
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
         int local = 0;
-        for (int e = e0; e < e1; ++e) local += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+        for (int e = e0; e < e1; ++e) local += (s_off[e + 1] - s_off[e] + C::TILE_M - 1) / C::TILE_M;
         int incl = local;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -293,12 +404,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         int run = incl - local;
         for (int e = e0; e < e1; ++e) {
             s_tile[e] = run;
-            run += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+            run += (s_off[e + 1] - s_off[e] + C::TILE_M - 1) / C::TILE_M;
         }
         if (lane == 31) s_tile[E] = incl;
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // both CTAs' barriers and tensor memory are ready
     tc_fence_after();
 
     const uint32_t tmem_base = *s_tmem;
@@ -310,11 +422,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         // ------------------------- TMA producer -------------------------
         int s = 0;
         uint32_t ph = 0;
-        uint32_t issued = 0, last_par = 0;  // per stage: ever issued, parity of last issue
+        uint32_t issued = 0, last_par = 0;  // per stage armed here: ever / parity of last phase
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles);
-            const int n0 = ti.n_blk * (SWIGLU ? BN / 2 : BN);
+        for (int tile = unit; tile < total && ok; tile += nunits) {
+            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles, C::TILE_M);
+            // first B column of this CTA: in G1 the gate columns come first and the
+            // up columns (offset f) follow; a pair splits them between its CTAs
+            int n0;
+            if (SWIGLU) n0 = ti.n_blk * (BN / 2) + (PAIR && !leader ? p.f : 0);
+            else n0 = ti.n_blk * BN + (int)rank * (BN / 2);
+            const int arow = ti.row0 + (int)rank * BM;
             for (int ks = 0; ks < nk; ++ks) {
                 int good = 1;
                 if (lane == 0) good = wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort);
@@ -324,22 +441,21 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     break;
                 }
                 if (lane == 0) {
-                    const uint32_t fb = bar_full + 8 * s;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    const int k0 = ks * BK;
-                    tma_load_2d(base_s + OFF_A + s * A_BYTES, &tmA, k0, ti.row0, fb);
-                    const uint32_t bdst = base_s + OFF_B + s * B_BYTES;
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) {
-                        int col;
-                        if (SWIGLU)
-                            col = (a < 2) ? (n0 + 64 * a) : (p.f + n0 + 64 * (a - 2));
-                        else
-                            col = n0 + 64 * a;
-                        tma_load_3d(bdst + a * B_ATOM_BYTES, &tmB, col, k0, ti.e, fb);
+                    if (leader) {
+                        mbar_arrive_expect_tx(bar_full + 8 * s, C::EXPECT_BYTES);
+                        issued |= 1u << s;
+                        last_par = (last_par & ~(1u << s)) | (ph << s);
                     }
-                    issued |= 1u << s;
-                    last_par = (last_par & ~(1u << s)) | (ph << s);
+                    const uint32_t fb = sig_full + 8 * s;
+                    const int k0 = ks * BK;
+                    tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, &tmA, k0, arow, fb);
+                    const uint32_t bdst = base_s + C::OFF_B + s * C::B_BYTES;
+#pragma unroll
+                    for (int a = 0; a < C::B_ATOMS; ++a) {
+                        int col = n0 + 64 * a;
+                        if (SWIGLU && !PAIR && a >= 2) col = ti.n_blk * (BN / 2) + p.f + 64 * (a - 2);
+                        tma_load_3d<CTAS>(bdst + a * B_ATOM_BYTES, &tmB, col, k0, ti.e, fb);
+                    }
                 }
                 __syncwarp();
                 if (++s == STAGES) {
@@ -348,8 +464,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 }
             }
         }
-        // drain: every issued load must have landed before the CTA exits
-        if (lane == 0) {
+        // drain: every phase armed here must have received all of its bytes
+        if (leader && lane == 0) {
             for (int i = 0; i < STAGES; ++i)
                 if ((issued >> i) & 1u) {
                     volatile int never = 0;
@@ -359,67 +475,73 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------- MMA issuer ---------------------------
-        int s = 0;
-        uint32_t ph = 0;
-        int it = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-            const int acc = it & 1;
-            const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-            int good = 1;
-            if (lane == 0) good = wait_bounded(bar_tempty + 8 * acc, aph ^ 1u, p.ds, s_abort);
-            good = __shfl_sync(0xffffffffu, good, 0);
-            if (!good) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-            for (int ks = 0; ks < nk; ++ks) {
-                good = 1;
-                if (lane == 0) good = wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort);
+        if (leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            bool ok = true;
+            // Descriptors of stage 0, K step 0; a stage / K step only moves
+            // the start address (bits 0-13, 16-byte units), so later ones are
+            // adds.  A: K-major, 128-byte rows, 8-row groups 1024 B apart; a
+            // K step of 16 elements is 32 bytes along the row.  B: MN-major,
+            // 64-column atoms 8 KB apart (LBO), 8-row K groups 1024 B apart
+            // (SBO); a K step of 16 rows is 2 KB.  In a pair the peer CTA's
+            // operands sit at the same offsets in its shared memory.
+            const uint64_t adesc0 = smem_desc_sw128(base_s + C::OFF_A, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(base_s + C::OFF_B, B_ATOM_BYTES, 1024);
+            for (int tile = unit; tile < total && ok; tile += nunits, ++it) {
+                const int acc = it & 1;
+                const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                int good = 1;
+                if (lane == 0) good = wait_bounded(bar_tempty + 8 * acc, aph ^ 1u, p.ds, s_abort);
                 good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
+                if (!good) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_s = base_s + OFF_A + s * A_BYTES;
-                    const uint32_t b_s = base_s + OFF_B + s * B_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        // A: K-major, 128-byte rows, 8-row groups 1024 B apart;
-                        //    K step of 16 elements = 32 bytes along the row.
-                        const uint64_t adesc = smem_desc_sw128(a_s + kk * 32, 16, 1024);
-                        // B: MN-major, 64-column atoms 8 KB apart (LBO), 8-row K
-                        //    groups 1024 B apart (SBO); K step of 16 rows = 2 KB.
-                        const uint64_t bdesc = smem_desc_sw128(b_s + kk * 2048, B_ATOM_BYTES, 1024);
-                        mma_bf16(d_tmem, adesc, bdesc, (ks | kk) != 0 ? 1u : 0u);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int ks = 0; ks < nk; ++ks) {
+                    good = 1;
+                    if (lane == 0) good = wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort);
+                    good = __shfl_sync(0xffffffffu, good, 0);
+                    if (!good) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(bar_empty + 8 * s);  // frees the stage once these MMAs finish
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint64_t a_st = adesc0 + (uint64_t)((s * A_BYTES) >> 4);
+                        const uint64_t b_st = bdesc0 + (uint64_t)((s * C::B_BYTES) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                            mma_bf16<CTAS>(d_tmem, a_st + (uint64_t)((kk * 32) >> 4),
+                                           b_st + (uint64_t)((kk * 2048) >> 4),
+                                           (ks | kk) != 0 ? 1u : 0u);
+                        mma_commit_all<CTAS>(bar_empty + 8 * s);  // frees the stage (both CTAs)
+                    }
+                    __syncwarp();
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
+                if (!ok) break;
+                if (lane == 0) mma_commit_all<CTAS>(bar_tfull + 8 * acc);  // accumulators ready
                 __syncwarp();
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(bar_tfull + 8 * acc);  // accumulator ready
+            // drain: every MMA issued here completes before tensor memory is freed
+            if (lane == 0) {
+                mma_commit_local<CTAS>(bar_drain);
+                volatile int never = 0;
+                wait_bounded(bar_drain, 0, p.ds, &never);
+            }
             __syncwarp();
         }
-        // drain: all MMAs issued by this thread complete before tensor memory is freed
-        if (lane == 0) {
-            mma_commit(bar_drain);
-            volatile int never = 0;
-            wait_bounded(bar_drain, 0, p.ds, &never);
-        }
-        __syncwarp();
     } else {
         // --------------------------- epilogue ----------------------------
         const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
-        const int r_in_tile = quarter * 32 + lane;
+        const int r_in_tile = (int)rank * BM + quarter * 32 + lane;
         int it = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles);
+        for (int tile = unit; tile < total; tile += nunits, ++it) {
+            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles, C::TILE_M);
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             const int good = __all_sync(0xffffffffu,
@@ -484,14 +606,18 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_tempty + 8 * acc);
+            if (lane == 0) {  // the MMA issuer may reuse this accumulator
+                if (PAIR) mbar_arrive_cluster(sig_tempty + 8 * acc);
+                else mbar_arrive(bar_tempty + 8 * acc);
+            }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc<CTAS>(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------ host side ----------------------------------
@@ -541,8 +667,78 @@ bool make_map_weights(CUtensorMap *m, const void *ptr, int64_t E, int64_t K, int
 
 struct DeviceInfo {
     bool ready = false;
-    int sms = 0;
+    int sms = 0;    // single CTAs that fit at once (one per SM)
+    int pairs = 0;  // CTA pairs that fit at once
 };
+
+template <bool SWIGLU, int CTAS>
+cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CTAS>::SMEM_BYTES;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CTAS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <bool SWIGLU, int CTAS>
+cudaError_t launch(unsigned grid, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p,
+                   cudaStream_t st) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config<SWIGLU, CTAS>(grid, st, attr);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, CTAS>, ta, tb, p);
+}
+
+template <bool SWIGLU, int CTAS> cudaError_t prepare(int *resident_units) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, CTAS>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Cfg<CTAS>::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config<SWIGLU, CTAS>(CTAS, nullptr, attr);
+    return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<SWIGLU, CTAS>, &cfg);
+}
+
+template <int CTAS>
+cudaError_t run(const Shape &s, int units, const CUtensorMap &mx, const CUtensorMap &mwgu,
+                const CUtensorMap &mh, const CUtensorMap &mwd, const int32_t *offsets,
+                void *h_perm, void *y_perm, const DevStatus &ds, cudaStream_t st) {
+    const int64_t P = s.P();
+    constexpr int TM = Cfg<CTAS>::TILE_M;
+    // Upper bound of the row tiles: sum_e ceil(count_e/TM) <= P/TM + min(E, P).
+    const int64_t row_tiles_max = (P + TM - 1) / TM + std::min<int64_t>(s.E, P);
+    const int64_t n_tiles1 = (s.f + BN / 2 - 1) / (BN / 2), n_tiles2 = (s.d + BN - 1) / BN;
+    if (row_tiles_max * std::max(n_tiles1, n_tiles2) >= (int64_t)INT32_MAX) {
+        set_error_message("grouped GEMM tile count exceeds 2^31");
+        return cudaErrorInvalidValue;
+    }
+    Params p1;
+    p1.offsets = offsets;
+    p1.E = s.E;
+    p1.K = s.d;
+    p1.n_out = s.f;
+    p1.f = s.f;
+    p1.n_tiles = (int)n_tiles1;
+    p1.out = static_cast<__nv_bfloat16 *>(h_perm);
+    p1.ds = ds;
+    const unsigned g1 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles1);
+    cudaError_t err = launch<true, CTAS>(g1, mx, mwgu, p1, st);
+    if (err != cudaSuccess) return err;
+    Params p2 = p1;
+    p2.K = s.f;
+    p2.n_out = s.d;
+    p2.f = 0;
+    p2.n_tiles = (int)n_tiles2;
+    p2.out = static_cast<__nv_bfloat16 *>(y_perm);
+    const unsigned g2 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles2);
+    return launch<false, CTAS>(g2, mh, mwd, p2, st);
+}
 
 }  // namespace tc
 
@@ -556,17 +752,16 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!info[dev].ready) {
-        if ((err = cudaDeviceGetAttribute(&info[dev].sms, cudaDevAttrMultiProcessorCount, dev)) !=
-            cudaSuccess)
+        int a = 0, b = 0, c = 0, d = 0;
+        if ((err = prepare<true, 1>(&a)) != cudaSuccess || (err = prepare<false, 1>(&b)) != cudaSuccess ||
+            (err = prepare<true, 2>(&c)) != cudaSuccess || (err = prepare<false, 2>(&d)) != cudaSuccess)
             return err;
-        if ((err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES)) != cudaSuccess)
-            return err;
-        if ((err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        SMEM_BYTES)) != cudaSuccess)
-            return err;
+        info[dev].sms = std::min(a, b);
+        info[dev].pairs = std::min(c, d);
+        if (info[dev].sms < 1 || info[dev].pairs < 1) {
+            set_error_message("the grouped GEMM does not fit on device %d", dev);
+            return cudaErrorInvalidConfiguration;
+        }
         info[dev].ready = true;
     }
     if (!encode_fn()) {
@@ -580,37 +775,11 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
         set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
         return cudaErrorInvalidValue;
     }
-    // Upper bound of the row tiles (sum_e ceil(count_e/BM) <= P/BM + E) times the column tiles.
-    const int64_t row_tiles_max = (P + BM - 1) / BM + std::min<int64_t>(s.E, P);
-
-    Params p1;
-    p1.offsets = offsets;
-    p1.E = s.E;
-    p1.K = s.d;
-    p1.n_out = s.f;
-    p1.f = s.f;
-    p1.n_tiles = (s.f + BN / 2 - 1) / (BN / 2);
-    p1.out = static_cast<__nv_bfloat16 *>(h_perm);
-    p1.ds = ds;
-    int64_t bound1 = row_tiles_max * p1.n_tiles;
-    if (bound1 >= (int64_t)INT32_MAX || row_tiles_max * ((s.d + BN - 1) / BN) >= (int64_t)INT32_MAX) {
-        set_error_message("grouped GEMM tile count exceeds 2^31");
-        return cudaErrorInvalidValue;
-    }
-    unsigned grid1 = (unsigned)std::min<int64_t>(info[dev].sms, bound1);
-    grouped_gemm_tc_kernel<true><<<grid1, NUM_THREADS, SMEM_BYTES, st>>>(mx, mwgu, p1);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-
-    Params p2 = p1;
-    p2.K = s.f;
-    p2.n_out = s.d;
-    p2.f = 0;
-    p2.n_tiles = (s.d + BN - 1) / BN;
-    p2.out = static_cast<__nv_bfloat16 *>(y_perm);
-    int64_t bound2 = row_tiles_max * p2.n_tiles;
-    unsigned grid2 = (unsigned)std::min<int64_t>(info[dev].sms, bound2);
-    grouped_gemm_tc_kernel<false><<<grid2, NUM_THREADS, SMEM_BYTES, st>>>(mh, mwd, p2);
-    return cudaGetLastError();
+    // Pairs (256-row tiles) when experts average >= 512 rows; else 128-row
+    // tiles, which waste less on ragged segments and small batches.
+    if (P >= (int64_t)kPairRowsPerExpert * s.E)
+        return run<2>(s, info[dev].pairs, mx, mwgu, mh, mwd, offsets, h_perm, y_perm, ds, st);
+    return run<1>(s, info[dev].sms, mx, mwgu, mh, mwd, offsets, h_perm, y_perm, ds, st);
 }
 
 }  // namespace moe
