@@ -234,6 +234,16 @@ moe_status_t moe_last_device_error(void *stream);
  */
 void moe_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Test hook for the failure path (no counterpart on the pages).  While
+ * enabled (non-zero), every later tensor-core grouped GEMM launch first waits
+ * on a barrier that nothing signals, so that wait runs out after the wait
+ * limit: the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its in-flight
+ * copies, frees its tensor memory and returns without computing.  The
+ * outputs of such a call are undefined.  Off by default.
+ */
+void moe_debug_inject_wait_timeout(int enable);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,6 +15,7 @@ constexpr unsigned kErrBadRouting = 2u;
 struct DevStatus {
     unsigned *err;          // device error word (never null)
     unsigned long long wait_limit_ns;  // bound on each device-side wait
+    int inject_wait_timeout;  // test hook: the GEMM waits on a barrier nothing signals
 };
 
 __device__ __forceinline__ void raise_error(const DevStatus &st, unsigned bit) {

@@ -301,7 +301,8 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 // Bounded wait: true when the phase with `parity` has completed; false when
 // the limit ran out or another role raised the abort flag.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
-                                             volatile int *abort_flag) {
+                                             volatile int *abort_flag,
+                                             unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
@@ -309,12 +310,21 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > ds.wait_limit_ns) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             raise_error(ds, kErrTimeout);
             *abort_flag = 1;
             return false;
         }
     }
+}
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
+                                             volatile int *abort_flag) {
+    return wait_bounded(bar, parity, ds, abort_flag, ds.wait_limit_ns);
+}
+// Drain waits (in-flight copies / MMAs before the CTA frees its resources)
+// never use less than 1 s, whatever limit the caller set for the main loop.
+__device__ __forceinline__ unsigned long long drain_limit(const DevStatus &ds) {
+    return ds.wait_limit_ns > 1000000000ull ? ds.wait_limit_ns : 1000000000ull;
 }
 
 struct TileInfo {
@@ -469,7 +479,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int i = 0; i < STAGES; ++i)
                 if ((issued >> i) & 1u) {
                     volatile int never = 0;
-                    if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never)) break;
+                    if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never,
+                                      drain_limit(p.ds)))
+                        break;
                 }
         }
         __syncwarp();
@@ -489,6 +501,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             // operands sit at the same offsets in its shared memory.
             const uint64_t adesc0 = smem_desc_sw128(base_s + C::OFF_A, 16, 1024);
             const uint64_t bdesc0 = smem_desc_sw128(base_s + C::OFF_B, B_ATOM_BYTES, 1024);
+            if (p.ds.inject_wait_timeout) {
+                // test hook: wait on the drain barrier, which nothing signals
+                // before the issuer's own final commit, so the wait runs out
+                // and the kernel takes its abort path before any MMA
+                int good = 1;
+                if (lane == 0) good = wait_bounded(bar_drain, 0, p.ds, s_abort);
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            }
             for (int tile = unit; tile < total && ok; tile += nunits, ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
@@ -531,7 +551,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             if (lane == 0) {
                 mma_commit_local<CTAS>(bar_drain);
                 volatile int never = 0;
-                wait_bounded(bar_drain, 0, p.ds, &never);
+                wait_bounded(bar_drain, 0, p.ds, &never, drain_limit(p.ds));
             }
             __syncwarp();
         }

@@ -26,6 +26,7 @@ const char *error_message() { return g_msg; }
 __device__ unsigned g_device_error_word;
 
 static std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+static std::atomic<int> g_inject_wait_timeout{0};
 
 namespace {
 
@@ -74,6 +75,7 @@ moe_status_t device_status(DevStatus *out) {
     if (!s.supported) return MOE_ERR_UNSUPPORTED;
     out->err = s.err_word;
     out->wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    out->inject_wait_timeout = g_inject_wait_timeout.load(std::memory_order_relaxed);
     return MOE_OK;
 }
 
@@ -218,6 +220,10 @@ size_t moe_dispatch_workspace_size(const moe_config_t *cfg) {
 
 void moe_set_wait_limit_ns(uint64_t ns) {
     g_wait_limit_ns.store(ns ? ns : 2000000000ull, std::memory_order_relaxed);
+}
+
+void moe_debug_inject_wait_timeout(int enable) {
+    g_inject_wait_timeout.store(enable ? 1 : 0, std::memory_order_relaxed);
 }
 
 moe_status_t moe_route(const moe_config_t *cfg, const void *x, const float *Wr,

@@ -64,6 +64,7 @@ def _load():
         "moe_forward_host": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "moe_last_device_error": ([vp], st),
         "moe_set_wait_limit_ns": ([ctypes.c_uint64], None),
+        "moe_debug_inject_wait_timeout": ([ctypes.c_int], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -134,6 +135,10 @@ def moe_dispatch_workspace_size(cfg: moe_config_t) -> int:
 
 def moe_set_wait_limit_ns(ns: int) -> None:
     _lib.moe_set_wait_limit_ns(int(ns))
+
+
+def moe_debug_inject_wait_timeout(enable: bool) -> None:
+    _lib.moe_debug_inject_wait_timeout(int(bool(enable)))
 
 
 def moe_route(cfg, x, Wr, logit_bias, logits, topk_idx, topk_w, stream=None, raise_on_error=True):
