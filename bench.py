@@ -354,12 +354,17 @@ def run_ours(args, w):
                     "frac_hbm": comb_bytes / kms["combine"] / 1e6 / hbm},
         "sum_ms": sum(kms.values()), "same_output_as_moe_forward": same_as_fused,
     }
-    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": gemm_tflops / peaks["bf16_tflops"],
+    # The GEMM runs back to back inside a long timed loop (power-capped
+    # clocks, see "clocks"), so its denominator is the sustained bf16 peak;
+    # the burst fraction is reported beside it.
+    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+    roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peak,
+                "unit": "TFLOP/s", "frac": gemm_tflops / peak,
+                "frac_of_burst_peak": gemm_tflops / peaks["bf16_tflops"],
                 "traffic": recorded_traffic(w), "kernel": "grouped_gemm_tc_kernel (G1 gate/up "
                 "+ SwiGLU, G2 down) via moe_grouped_swiglu",
                 "algorithmic": f"6*P*d*f = {gemm_flops:.4g} FLOP per call (P=T*k={P})",
-                "peak_source": peaks["source"] + " bf16_tflops (burst)"}
+                "peak_source": peaks["source"] + " bf16_tflops_sustained"}
 
     # ---- e2e: activations in pinned host memory, copies inside the region ----
     x_host = x.cpu().pin_memory()
@@ -413,8 +418,9 @@ def run_ours(args, w):
 
 
 def recorded_traffic(w):
-    """DRAM bytes per moe_grouped_swiglu call from the committed ncu summary,
-    if it was taken on this workload with the current kernel source."""
+    """DRAM bytes (read + write) per moe_grouped_swiglu call (G1 + G2) from
+    the committed ncu summary, if it was taken on this workload with the
+    current kernel source; else None."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "grouped_gemm_tc_traffic.json")
     src = os.path.join(ROOT, "token_dispatch_grouped_fp32_gb300", "csrc", "gemm_tc.cu")
