@@ -308,11 +308,12 @@ def run_ours(args, w):
     y_perm = torch.empty(P, w.d, dtype=x.dtype, device=dev)
     out2 = torch.empty_like(x)
     dws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device=dev)
+    rws = torch.empty(max(256, moe.moe_route_workspace_size(cfg)), dtype=torch.uint8, device=dev)
     names = ["route", "dispatch", "grouped_swiglu", "combine"]
 
     def parts(ev=None):
         if ev: ev[0].record(stream)
-        moe.moe_route(cfg, x, Wr, bias, logits, idx, wt, stream=stream)
+        moe.moe_route(cfg, x, Wr, bias, logits, idx, wt, rws, stream=stream)
         if ev: ev[1].record(stream)
         moe.moe_dispatch(cfg, idx, x, counts, offsets, pos, src, x_perm, dws, stream=stream)
         if ev: ev[2].record(stream)

@@ -85,14 +85,22 @@ const char *moe_last_error_message(void);
 
 /*
  * Bytes of workspace moe_forward needs for `cfg` (0 when T == 0).  The same
- * buffer also satisfies moe_dispatch.  The workspace holds the router
- * logits, routing, dispatch arrays and the permuted activations x_perm,
- * h_perm and y_perm; see moe_forward.
+ * buffer also satisfies moe_route and moe_dispatch.  The workspace holds the
+ * router logits and scratch, routing, dispatch arrays and the permuted
+ * activations x_perm, h_perm and y_perm; see moe_forward.
  */
 size_t moe_workspace_size(const moe_config_t *cfg);
 
 /* Bytes of workspace moe_dispatch needs for `cfg` (per-block histograms). */
 size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
+
+/*
+ * Bytes of workspace moe_route needs for `cfg`: 0 when the logits are
+ * computed on the CUDA cores (fp32 activations, E < 64 or E > 256, E not a
+ * multiple of 16, or d not a multiple of 64); otherwise the three-term bf16
+ * split of Wr (E * 3d * 2 bytes) and fp32 partial logits of the K splits.
+ */
+size_t moe_route_workspace_size(const moe_config_t *cfg);
 
 /*
  * Router [EP-add: the router yields top_k_index and top_k_weights].
@@ -108,11 +116,17 @@ size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
  * logit_bias [E]     fp32 or NULL: an additive per-expert logit offset
  * logits     [T][E]  fp32, written
  * topk_idx   [T][k]  int32, written; topk_w [T][k] fp32, written
+ * ws         at least moe_route_workspace_size(cfg) bytes, 256-byte aligned
+ *            (may be NULL when that size is 0)
  * The selection is made on exactly the fp32 values written to `logits`.
+ * For bf16 x with 64 <= E <= 256 (E % 16 == 0, d % 64 == 0) the products are
+ * formed on the tensor cores: Wr is split into three bf16 terms
+ * (w = w1 + w2 + w3, ~2^-25 relative), each product with the exact bf16 x is
+ * exact, and accumulation is fp32; otherwise fp32 FMAs on the CUDA cores.
  */
 moe_status_t moe_route(const moe_config_t *cfg, const void *x, const float *Wr,
                        const float *logit_bias, float *logits, int32_t *topk_idx,
-                       float *topk_w, void *stream);
+                       float *topk_w, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * The selection and weights of moe_route on a GIVEN fp32 logit buffer

@@ -96,7 +96,7 @@ def check_layer(moe, oracle, w, device="cuda", sample=None, max_experts=48, bias
     g_idx = torch.empty(w.T, w.k, dtype=torch.int32, device="cuda")
     g_w = torch.empty(w.T, w.k, dtype=torch.float32, device="cuda")
     g_L = torch.empty(w.T, w.E, dtype=torch.float32, device="cuda")
-    moe.moe_route(cfg, x, Wr, bias_d, g_L, g_idx, g_w)
+    moe.moe_route(cfg, x, Wr, bias_d, g_L, g_idx, g_w, layer.workspace(w.T))
     g_idx = g_idx.cpu().numpy()
 
     Wrs = f32(Wr)

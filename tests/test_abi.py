@@ -83,6 +83,21 @@ def test_null_and_misaligned_pointers(moe):
                            raise_on_error=False) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_route_workspace_size(moe):
+    # CUDA-core logits (E <= 32, or fp32 activations) need no workspace
+    assert moe.moe_route_workspace_size(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 0
+    assert moe.moe_route_workspace_size(moe.config(64, 128, 128, 2, 256, "f32")) == 0
+    # tensor-core logits: split weight (E*3d bf16) + fp32 partial logits
+    T, d, E = 8192, 7168, 256
+    n = moe.moe_route_workspace_size(moe.config(T, d, E, 8, 2048, "bf16"))
+    assert n >= E * 3 * d * 2 + T * E * 4
+    assert n <= E * 3 * d * 2 + 256 + 64 * T * E * 4
+    cfg = moe.config(T, d, E, 8, 2048, "bf16")
+    st = moe.moe_route(cfg, 16, 16, None, 16, 16, 16, 16, n - 1, stream=0, raise_on_error=False)
+    assert st == moe.MOE_ERR_WORKSPACE
+    assert moe.moe_workspace_size(cfg) >= n + 2 * T * 8 * (d + 2048 + d)
+
+
 def test_workspace_too_small(moe):
     cfg = moe.config(16, 64, 8, 2, 64)
     need = moe.moe_workspace_size(cfg)
@@ -96,7 +111,7 @@ def test_workspace_too_small(moe):
 def test_empty_batch_is_a_no_op(moe):
     cfg = moe.config(0, 64, 8, 2, 64)
     assert moe.moe_forward(cfg, 16, 16, None, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
-    assert moe.moe_route(cfg, 16, 16, None, 16, 16, 16, stream=0) == moe.MOE_OK
+    assert moe.moe_route(cfg, 16, 16, None, 16, 16, 16, None, 0, stream=0) == moe.MOE_OK
     assert moe.moe_dispatch(cfg, 16, 16, 16, 16, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
     assert moe.moe_grouped_swiglu(cfg, 16, 16, 16, 16, 16, 16, stream=0) == moe.MOE_OK
     assert moe.moe_combine(cfg, 16, 16, 16, 16, stream=0) == moe.MOE_OK

@@ -1,6 +1,8 @@
 """Router parity: top-k indices bit-exact and weights within the fp32 bound
 against the oracle on the same fp32 logit buffer; router logits within the
-fp32 summation bound."""
+fp32 summation bound, on both logit paths (CUDA-core FMAs for E <= 32 or
+fp32 x; tensor cores with the three-term bf16 split of Wr for bf16 x and
+64 <= E <= 256)."""
 import numpy as np
 import pytest
 import torch
@@ -50,7 +52,8 @@ def test_route_from_logits_matches_oracle(moe, oracle, T, E, k, ties, renorm):
 
 
 @pytest.mark.parametrize("name,T", [("tiny_fp32", 64), ("mixtral", 512), ("gptoss_prefill", 700),
-                                    ("qwen3_zipf", 1500), ("deepseek", 300)])
+                                    ("qwen3_zipf", 1500), ("deepseek", 300), ("gptoss_decode", 64),
+                                    ("deepseek", 8192)])
 def test_route_logits_and_selection(moe, oracle, name, T):
     w = synth.WORKLOADS[name].with_tokens(T)
     inp = synth.make_inputs(w, weights=False)
@@ -59,7 +62,9 @@ def test_route_logits_and_selection(moe, oracle, name, T):
     logits = torch.empty(T, w.E, dtype=torch.float32, device="cuda")
     idx = torch.empty(T, w.k, dtype=torch.int32, device="cuda")
     wt = torch.empty(T, w.k, dtype=torch.float32, device="cuda")
-    moe.moe_route(cfg, x.cuda(), Wr.cuda(), None if bias is None else bias.cuda(), logits, idx, wt)
+    ws = torch.empty(max(256, moe.moe_route_workspace_size(cfg)), dtype=torch.uint8, device="cuda")
+    moe.moe_route(cfg, x.cuda(), Wr.cuda(), None if bias is None else bias.cuda(), logits, idx, wt,
+                  ws)
     torch.cuda.synchronize()
     xs, Wrs = f32(x), f32(Wr)
     bs = None if bias is None else f32(bias)

@@ -54,6 +54,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace tc {
@@ -87,15 +88,7 @@ template <int CTAS> struct Cfg {
     static constexpr int OFF_OFFS = OFF_ABORT + 4;               // int[MAX_E + 1]
     static constexpr int OFF_TILE = OFF_OFFS + 4 * (MAX_E + 1);  // int[MAX_E + 1]
     static constexpr int SMEM_BYTES = OFF_TILE + 4 * (MAX_E + 1) + 1024;  // + alignment slack
-    // instruction descriptor of tcgen05.mma kind::f16: D fp32, A and B bf16,
-    // A K-major, B MN-major, M = TILE_M, N = 256
-    static constexpr uint32_t IDESC = (1u << 4)       // D format: f32
-                                      | (1u << 7)     // A format: bf16
-                                      | (1u << 10)    // B format: bf16
-                                      | (0u << 15)    // A major: K
-                                      | (1u << 16)    // B major: MN
-                                      | ((uint32_t)(BN >> 3) << 17)
-                                      | ((uint32_t)(TILE_M >> 4) << 24);
+    static constexpr uint32_t IDESC = idesc_bf16(TILE_M, BN, true);  // B MN-major
     static constexpr int EPI_ARRIVALS = 4 * CTAS;         // epilogue warps reporting per tile
 };
 
@@ -109,223 +102,6 @@ struct Params {
     __nv_bfloat16 *out;  // [P][n_out]
     DevStatus ds;
 };
-
-// ----------------------------- PTX wrappers --------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-// Address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-// Arrive on a barrier anywhere in the cluster (cluster-window address).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-                 : "memory");
-}
-// TMA tile loads into this CTA's shared memory.  CTAS = 1: completion on a
-// barrier of this CTA.  CTAS = 2: on a barrier of either CTA of the pair
-// (cluster-window address).
-template <int CTAS>
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
-                                            uint32_t bar) {
-    if constexpr (CTAS == 2)
-        asm volatile(
-            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
-            : "memory");
-    else
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(bar)
-            : "memory");
-}
-template <int CTAS>
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
-                                            int c2, uint32_t bar) {
-    if constexpr (CTAS == 2)
-        asm volatile(
-            "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-            : "memory");
-    else
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-            : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Tensor-memory allocation: one warp of the CTA (CTAS = 1), or one warp of
-// each CTA of the pair together (CTAS = 2).
-template <int CTAS> __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    if constexpr (CTAS == 2) {
-        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         dst_smem),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-    } else {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         dst_smem),
-                     "r"(ncols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-}
-template <int CTAS> __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    if constexpr (CTAS == 2)
-        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
-                     "r"(ncols)
-                     : "memory");
-    else
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr),
-                     "r"(ncols)
-                     : "memory");
-}
-template <int CTAS>
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
-    if constexpr (CTAS == 2)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(Cfg<2>::IDESC), "r"(accumulate)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "setp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(Cfg<1>::IDESC), "r"(accumulate)
-            : "memory");
-}
-// Arrive on the barrier at offset `bar` (in both CTAs of a pair) once this
-// thread's earlier MMAs have completed.
-template <int CTAS> __device__ __forceinline__ void mma_commit_all(uint32_t bar) {
-    if constexpr (CTAS == 2) {
-        const uint16_t mask = 0x3;
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-            " [%0], %1;" ::"r"(bar), "h"(mask)
-            : "memory");
-    } else {
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-            : "memory");
-    }
-}
-// ... on this CTA's barrier only.
-template <int CTAS> __device__ __forceinline__ void mma_commit_local(uint32_t bar) {
-    if constexpr (CTAS == 2)
-        asm volatile(
-            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-            : "memory");
-    else
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-            : "memory");
-}
-// 32 lanes x 32 consecutive fp32 columns: thread i gets lane (base + i).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05 format): start address, leading
-// and stride byte offsets (16-byte units), version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-    d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;  // swizzle: 128 B
-    return d;
-}
-
-// Bounded wait: true when the phase with `parity` has completed; false when
-// the limit ran out or another role raised the abort flag.
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
-                                             volatile int *abort_flag,
-                                             unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > limit_ns) {
-            raise_error(ds, kErrTimeout);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
-                                             volatile int *abort_flag) {
-    return wait_bounded(bar, parity, ds, abort_flag, ds.wait_limit_ns);
-}
-// Drain waits (in-flight copies / MMAs before the CTA frees its resources)
-// never use less than 1 s, whatever limit the caller set for the main loop.
-__device__ __forceinline__ unsigned long long drain_limit(const DevStatus &ds) {
-    return ds.wait_limit_ns > 1000000000ull ? ds.wait_limit_ns : 1000000000ull;
-}
 
 struct TileInfo {
     int e, row0, rows, n_blk;  // row0/rows: the tile's slice of expert e's segment
@@ -533,7 +309,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                         for (int kk = 0; kk < BK / UMMA_K; ++kk)
                             mma_bf16<CTAS>(d_tmem, a_st + (uint64_t)((kk * 32) >> 4),
-                                           b_st + (uint64_t)((kk * 2048) >> 4),
+                                           b_st + (uint64_t)((kk * 2048) >> 4), C::IDESC,
                                            (ks | kk) != 0 ? 1u : 0u);
                         mma_commit_all<CTAS>(bar_empty + 8 * s);  // frees the stage (both CTAs)
                     }

@@ -22,6 +22,24 @@ cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr,
 // Top-k selection and softmax weights on a given fp32 logit buffer.
 cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
                         cudaStream_t st);
+// Top-k on logits formed as sum of `splits` partial buffers [splits][T][E]
+// (added in split order) plus bias; the logits are written to `logits`.
+cudaError_t launch_topk_partials(const Shape &s, const float *partial, int splits,
+                                 const float *bias, float *logits, int32_t *idx, float *w,
+                                 cudaStream_t st);
+
+// Router logits on the tensor cores (bf16 x, fp32 Wr split into 3 bf16 terms).
+struct RouterTcPlan {
+    int ks_total;      // K steps of 64 over K' = 3d
+    int ks_per_split;  // K steps per CTA
+    int splits;        // K splits (blockIdx.y)
+};
+bool router_tc_eligible(const Shape &s);
+RouterTcPlan router_tc_plan(const Shape &s);
+size_t router_tc_scratch_bytes(const Shape &s);  // split weight + partial logits
+cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *Wr, void *scratch,
+                                    float **partial_out, int *splits_out, const DevStatus &ds,
+                                    cudaStream_t st);
 
 // Dispatch: chunking of the P pairs over histogram/scatter blocks.
 struct DispatchGrid {

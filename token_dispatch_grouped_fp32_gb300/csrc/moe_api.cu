@@ -142,7 +142,7 @@ moe_status_t from_cuda(cudaError_t e, const char *what) {
 
 // ----- workspace layout of moe_forward (256-byte aligned sub-buffers) -----
 struct WsLayout {
-    size_t logits, idx, w, counts, offsets, pos, src, hist, x_perm, h_perm, y_perm, total;
+    size_t logits, idx, w, counts, offsets, pos, src, hist, route, x_perm, h_perm, y_perm, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -159,6 +159,7 @@ WsLayout ws_layout(const Shape &s) {
     L.pos = o;    o = up256(o + 4 * P);
     L.src = o;    o = up256(o + 4 * P);
     L.hist = o;   o = up256(o + dispatch_scratch_bytes(s));
+    L.route = o;  o = up256(o + router_tc_scratch_bytes(s));
     L.x_perm = o; o = up256(o + es * P * s.d);
     L.h_perm = o; o = up256(o + es * P * s.f);
     L.y_perm = o; o = up256(o + es * P * s.d);
@@ -168,6 +169,27 @@ WsLayout ws_layout(const Shape &s) {
 
 template <typename T> T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+// Router: tensor-core logits (split weight, K-split partials summed by the
+// top-k kernel) when the shape allows, else the SIMT logits kernel.
+moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const float *bias,
+                       float *logits, int32_t *idx, float *w, void *route_ws,
+                       const DevStatus &ds, cudaStream_t st) {
+    if (router_tc_eligible(s)) {
+        float *partial = nullptr;
+        int splits = 0;
+        moe_status_t r = from_cuda(
+            launch_router_logits_tc(s, x, Wr, route_ws, &partial, &splits, ds, st),
+            "router logits launch");
+        if (r != MOE_OK) return r;
+        return from_cuda(launch_topk_partials(s, partial, splits, bias, logits, idx, w, st),
+                         "top-k launch");
+    }
+    moe_status_t r = from_cuda(launch_router_logits(s, x, Wr, bias, logits, st),
+                               "router logits launch");
+    if (r != MOE_OK) return r;
+    return from_cuda(launch_topk(s, logits, idx, w, st), "top-k launch");
 }
 
 moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offsets,
@@ -212,6 +234,12 @@ size_t moe_workspace_size(const moe_config_t *cfg) {
     return ws_layout(s).total;
 }
 
+size_t moe_route_workspace_size(const moe_config_t *cfg) {
+    Shape s;
+    if (check_cfg(cfg, &s) != MOE_OK || s.T == 0) return 0;
+    return router_tc_scratch_bytes(s);
+}
+
 size_t moe_dispatch_workspace_size(const moe_config_t *cfg) {
     Shape s;
     if (check_cfg(cfg, &s) != MOE_OK || s.T == 0) return 0;
@@ -228,7 +256,7 @@ void moe_debug_inject_wait_timeout(int enable) {
 
 moe_status_t moe_route(const moe_config_t *cfg, const void *x, const float *Wr,
                        const float *logit_bias, float *logits, int32_t *topk_idx, float *topk_w,
-                       void *stream) {
+                       void *ws, size_t ws_bytes, void *stream) {
     g_msg[0] = 0;
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
@@ -239,12 +267,18 @@ moe_status_t moe_route(const moe_config_t *cfg, const void *x, const float *Wr,
         set_error_message("logit_bias is not 16-byte aligned");
         return MOE_ERR_INVALID_ARG;
     }
+    const size_t need = router_tc_scratch_bytes(s);
+    if (need > 0) {
+        if ((st = check_ptrs({ws})) != MOE_OK) return st;
+        if (ws_bytes < need) {
+            set_error_message("workspace %zu bytes < %zu needed", ws_bytes, need);
+            return MOE_ERR_WORKSPACE;
+        }
+    }
     DevStatus ds;
     if ((st = device_status(&ds)) != MOE_OK) return st;
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if ((st = from_cuda(launch_router_logits(s, x, Wr, logit_bias, logits, cs), "router logits launch")) != MOE_OK)
-        return st;
-    return from_cuda(launch_topk(s, logits, topk_idx, topk_w, cs), "top-k launch");
+    return run_route(s, x, Wr, logit_bias, logits, topk_idx, topk_w, ws, ds,
+                     static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits, int32_t *topk_idx,
@@ -342,9 +376,9 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
     void *x_perm = at<uint8_t>(ws, L.x_perm), *h_perm = at<uint8_t>(ws, L.h_perm),
          *y_perm = at<uint8_t>(ws, L.y_perm);
 
-    if ((st = from_cuda(launch_router_logits(s, x, Wr, logit_bias, logits, cs), "router logits launch")) != MOE_OK)
+    if ((st = run_route(s, x, Wr, logit_bias, logits, idx, w, at<uint8_t>(ws, L.route), ds, cs)) !=
+        MOE_OK)
         return st;
-    if ((st = from_cuda(launch_topk(s, logits, idx, w, cs), "top-k launch")) != MOE_OK) return st;
     if ((st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm,
                                         at<int32_t>(ws, L.hist), ds, cs),
                         "dispatch launch")) != MOE_OK)

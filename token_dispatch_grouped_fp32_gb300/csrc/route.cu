@@ -274,22 +274,38 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
 
 constexpr int kNoExpert = 0x7fffffff;
 
+// With nparts > 0 the logits are first formed as the sum of nparts partial
+// buffers (stride T*E, added in buffer order) plus bias, and written to
+// `logits`; the selection then uses exactly the written values.
 template <int VPL>
 __global__ void __launch_bounds__(256)
-topk_kernel(const float *__restrict__ logits, int64_t T, int E, int k, int renorm,
+topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int nparts,
+            const float *__restrict__ bias, int64_t T, int E, int k, int renorm,
             int32_t *__restrict__ idx, float *__restrict__ w) {
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
-    const float *L = logits + t * E;
+    float *L = logits + t * E;
 
     float v[VPL];
     unsigned avail = 0;  // bit i: value i of this lane is a not-yet-chosen expert
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
         int e = lane + 32 * i;
-        v[i] = (e < E) ? L[e] : -INFINITY;
-        if (e < E) avail |= 1u << i;
+        if (e < E) {
+            if (nparts > 0) {
+                float a = partial[t * E + e];
+                for (int q = 1; q < nparts; ++q) a += partial[(int64_t)q * T * E + t * E + e];
+                if (bias) a += bias[e];
+                L[e] = a;
+                v[i] = a;
+            } else {
+                v[i] = L[e];
+            }
+            avail |= 1u << i;
+        } else {
+            v[i] = -INFINITY;
+        }
     }
 
     float my_v = 0.f;
@@ -348,11 +364,22 @@ topk_kernel(const float *__restrict__ logits, int64_t T, int E, int k, int renor
 }
 
 template <int VPL>
-cudaError_t launch_topk_v(const Shape &s, const float *logits, int32_t *idx, float *w,
-                          cudaStream_t st) {
+cudaError_t launch_topk_v(const Shape &s, float *logits, const float *partial, int nparts,
+                          const float *bias, int32_t *idx, float *w, cudaStream_t st) {
     unsigned blocks = (unsigned)((s.T + 7) / 8);
-    topk_kernel<VPL><<<blocks, 256, 0, st>>>(logits, s.T, s.E, s.k, s.renorm ? 1 : 0, idx, w);
+    topk_kernel<VPL><<<blocks, 256, 0, st>>>(logits, partial, nparts, bias, s.T, s.E, s.k,
+                                             s.renorm ? 1 : 0, idx, w);
     return cudaGetLastError();
+}
+
+cudaError_t launch_topk_any(const Shape &s, float *logits, const float *partial, int nparts,
+                            const float *bias, int32_t *idx, float *w, cudaStream_t st) {
+    if (s.E <= 32) return launch_topk_v<1>(s, logits, partial, nparts, bias, idx, w, st);
+    if (s.E <= 64) return launch_topk_v<2>(s, logits, partial, nparts, bias, idx, w, st);
+    if (s.E <= 128) return launch_topk_v<4>(s, logits, partial, nparts, bias, idx, w, st);
+    if (s.E <= 256) return launch_topk_v<8>(s, logits, partial, nparts, bias, idx, w, st);
+    if (s.E <= 512) return launch_topk_v<16>(s, logits, partial, nparts, bias, idx, w, st);
+    return launch_topk_v<32>(s, logits, partial, nparts, bias, idx, w, st);
 }
 
 }  // namespace
@@ -367,12 +394,14 @@ cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr,
 
 cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
                         cudaStream_t st) {
-    if (s.E <= 32) return launch_topk_v<1>(s, logits, idx, w, st);
-    if (s.E <= 64) return launch_topk_v<2>(s, logits, idx, w, st);
-    if (s.E <= 128) return launch_topk_v<4>(s, logits, idx, w, st);
-    if (s.E <= 256) return launch_topk_v<8>(s, logits, idx, w, st);
-    if (s.E <= 512) return launch_topk_v<16>(s, logits, idx, w, st);
-    return launch_topk_v<32>(s, logits, idx, w, st);
+    // nparts == 0: the kernel only reads `logits`
+    return launch_topk_any(s, const_cast<float *>(logits), nullptr, 0, nullptr, idx, w, st);
+}
+
+cudaError_t launch_topk_partials(const Shape &s, const float *partial, int splits,
+                                 const float *bias, float *logits, int32_t *idx, float *w,
+                                 cudaStream_t st) {
+    return launch_topk_any(s, logits, partial, splits, bias, idx, w, st);
 }
 
 }  // namespace moe

@@ -1,0 +1,316 @@
+// router_tc.cu -- router logits on the sm_103a tensor cores, for bf16
+// activations and 64 <= E <= 256 experts.
+//
+// Transformers docs "Expert parallelism", section "Adding an implementation":
+// the router produces the logits from which top_k_index and top_k_weights are
+// chosen; the logits are fp32:  L[t][e] = sum_i x[t][i] * Wr[e][i].
+//
+// x is bf16, so it is exact as an MMA operand.  The fp32 router weight is
+// split into three bf16 terms, w = w1 + w2 + w3 with w1 = bf16(w),
+// w2 = bf16(w - w1), w3 = bf16(w - w1 - w2) (each difference is exact in
+// fp32), which carries w to about 2^-25 relative.  Every product x * w_j is
+// exact in the MMA's fp32 accumulator, so
+//     L = x . w1 + x . w2 + x . w3
+// is an fp32-accumulated dot product of x with w, like the SIMT kernel's,
+// at a fraction of its cost.  The three terms are laid side by side along K
+// (W' = [w1 | w2 | w3], E x 3d), so the router is one GEMM with K' = 3d whose
+// A tile at k' is x's tile at k' mod d.
+//
+// Layout: A = x (K-major, TMA box 64 x 128 tokens), B = W' (K-major, box
+// 64 x E), M = 128 tokens, N = E, K step 64, four pipeline stages.  K' is
+// split over blockIdx.y so the grid fills the GPU; each split writes fp32
+// partial logits [split][T][E], which the top-k kernel adds in split order
+// (a fixed order, so results are reproducible) before selecting.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int RBM = 128;   // tokens per tile (MMA M)
+constexpr int RBK = 64;    // K elements per stage (128 bytes of bf16)
+constexpr int RSTAGES = 4;
+constexpr int R_A_BYTES = RBM * RBK * 2;        // 16 KB
+constexpr int R_B_MAX_BYTES = 256 * RBK * 2;    // 32 KB for E = 256
+constexpr int R_THREADS = 128;
+constexpr int R_OFF_A = 0;
+constexpr int R_OFF_B = RSTAGES * R_A_BYTES;
+constexpr int R_OFF_BAR = R_OFF_B + RSTAGES * R_B_MAX_BYTES;
+constexpr int R_NUM_BARS = 2 * RSTAGES + 2;  // full, empty, done, drain
+constexpr int R_OFF_TMEM = R_OFF_BAR + R_NUM_BARS * 8;
+constexpr int R_OFF_ABORT = R_OFF_TMEM + 4;
+constexpr int R_SMEM_BYTES = R_OFF_ABORT + 4 + 1024;
+
+// W'[e][j*d + i] = j-th bf16 term of Wr[e][i], j = 0, 1, 2.
+__global__ void split_router_weight_kernel(const float *__restrict__ Wr, int64_t n, int d,
+                                           __nv_bfloat16 *__restrict__ Wsplit) {
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
+         q += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t e = q / d, i = q - e * d;
+        const float w = Wr[q];
+        const __nv_bfloat16 w1 = __float2bfloat16_rn(w);
+        const float r1 = w - __bfloat162float(w1);
+        const __nv_bfloat16 w2 = __float2bfloat16_rn(r1);
+        const float r2 = r1 - __bfloat162float(w2);
+        const __nv_bfloat16 w3 = __float2bfloat16_rn(r2);
+        __nv_bfloat16 *row = Wsplit + e * 3 * (int64_t)d;
+        row[i] = w1;
+        row[d + i] = w2;
+        row[2 * (int64_t)d + i] = w3;
+    }
+}
+
+struct RouterParams {
+    float *partial;   // [splits][T][E]
+    int64_t T;
+    int d, E;
+    int ks_per_split, ks_total;
+    uint32_t idesc;
+    uint32_t tmem_cols;
+    DevStatus ds;
+};
+
+__global__ void __launch_bounds__(R_THREADS, 1)
+router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                        const __grid_constant__ CUtensorMap tmW, RouterParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_s - raw_s);
+    const uint32_t bar_full = base_s + R_OFF_BAR;
+    const uint32_t bar_empty = bar_full + 8 * RSTAGES;
+    const uint32_t bar_done = bar_empty + 8 * RSTAGES;
+    const uint32_t bar_drain = bar_done + 8;
+    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + R_OFF_TMEM);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(base + R_OFF_ABORT);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)blockIdx.x * RBM;
+    const int split = blockIdx.y;
+    const int ks0 = split * p.ks_per_split;
+    const int ks1 = min(ks0 + p.ks_per_split, p.ks_total);
+    const uint32_t b_bytes = (uint32_t)p.E * RBK * 2;
+
+    if (threadIdx.x == 0) {
+        *s_abort = 0;
+        for (int i = 0; i < RSTAGES; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
+        }
+        mbar_init(bar_done, 1);
+        mbar_init(bar_drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) tmem_alloc<1>(base_s + R_OFF_TMEM, p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    bool mma_ok = true;
+
+    if (warp == 0) {
+        // ------------------------- TMA producer -------------------------
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, issued = 0, last_par = 0;
+            for (int ks = ks0; ks < ks1; ++ks) {
+                if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort)) break;
+                const uint32_t fb = bar_full + 8 * s;
+                mbar_arrive_expect_tx(fb, R_A_BYTES + b_bytes);
+                const int kp = ks * RBK;  // column of W' (K' = 3d)
+                tma_load_2d<1>(base_s + R_OFF_A + s * R_A_BYTES, &tmX, kp % p.d, (int)m0, fb);
+                tma_load_2d<1>(base_s + R_OFF_B + s * R_B_MAX_BYTES, &tmW, kp, 0, fb);
+                issued |= 1u << s;
+                last_par = (last_par & ~(1u << s)) | (ph << s);
+                if (++s == RSTAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            for (int i = 0; i < RSTAGES; ++i)  // drain: every armed copy lands
+                if ((issued >> i) & 1u) {
+                    volatile int never = 0;
+                    if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never,
+                                      drain_limit(p.ds)))
+                        break;
+                }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------- MMA issuer ---------------------------
+        if (lane == 0) {
+            // A and B are both K-major: 128-byte rows, 8-row groups 1024 B
+            // apart; a K step of 16 elements is 32 bytes along the row.
+            const uint64_t adesc0 = smem_desc_sw128(base_s + R_OFF_A, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(base_s + R_OFF_B, 16, 1024);
+            int s = 0;
+            uint32_t ph = 0;
+            for (int ks = ks0; ks < ks1; ++ks) {
+                if (!wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort)) {
+                    mma_ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t a_st = adesc0 + (uint64_t)((s * R_A_BYTES) >> 4);
+                const uint64_t b_st = bdesc0 + (uint64_t)((s * R_B_MAX_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < RBK / 16; ++kk)
+                    mma_bf16<1>(tmem, a_st + (uint64_t)((kk * 32) >> 4),
+                                b_st + (uint64_t)((kk * 32) >> 4), p.idesc,
+                                (ks > ks0 || kk > 0) ? 1u : 0u);
+                mma_commit_all<1>(bar_empty + 8 * s);
+                if (++s == RSTAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (mma_ok) mma_commit_all<1>(bar_done);
+            mma_commit_local<1>(bar_drain);  // drain before tensor memory is freed
+            volatile int never = 0;
+            wait_bounded(bar_drain, 0, p.ds, &never, drain_limit(p.ds));
+        }
+        __syncwarp();
+    }
+
+    // ----------------- epilogue: all four warps --------------------------
+    const int good = __all_sync(0xffffffffu, wait_bounded(bar_done, 0, p.ds, s_abort));
+    if (good) {
+        tc_fence_after();
+        const int64_t t = m0 + warp * 32 + lane;
+        float *row = p.partial + ((int64_t)split * p.T + t) * p.E;
+        const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+        for (int c = 0; c < p.E; c += 32) {
+            uint32_t v[32];
+            tmem_ld32(taddr + c, v);
+            tmem_ld_wait();
+            if (t < p.T) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4 *>(row + c + 4 * q) =
+                        make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc<1>(tmem, p.tmem_cols);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn router_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// rows x cols bf16 (cols contiguous), box 64 cols x box_rows rows, 128 B swizzle
+bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return router_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool router_tc_eligible(const Shape &s) {
+    return s.bf16 && s.E >= 64 && s.E <= 256 && s.E % 16 == 0 && s.d % RBK == 0;
+}
+
+RouterTcPlan router_tc_plan(const Shape &s) {
+    RouterTcPlan pl;
+    const int64_t tiles = (s.T + RBM - 1) / RBM;
+    pl.ks_total = 3 * s.d / RBK;
+    // enough CTAs for two per SM-wave of 152 SMs, at least 4 K steps each
+    int64_t want = (304 + tiles - 1) / tiles;
+    want = std::max<int64_t>(1, std::min<int64_t>(want, std::max(1, pl.ks_total / 4)));
+    pl.ks_per_split = (int)((pl.ks_total + want - 1) / want);
+    pl.splits = (pl.ks_total + pl.ks_per_split - 1) / pl.ks_per_split;
+    return pl;
+}
+
+size_t router_tc_scratch_bytes(const Shape &s) {
+    if (!router_tc_eligible(s) || s.T == 0) return 0;
+    const RouterTcPlan pl = router_tc_plan(s);
+    const size_t wsplit = ((size_t)s.E * 3 * s.d * 2 + 255) & ~(size_t)255;
+    return wsplit + (size_t)pl.splits * (size_t)s.T * s.E * 4;
+}
+
+cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *Wr, void *scratch,
+                                    float **partial_out, int *splits_out, const DevStatus &ds,
+                                    cudaStream_t st) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        if ((err = cudaFuncSetAttribute(router_logits_tc_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        R_SMEM_BYTES)) != cudaSuccess)
+            return err;
+        attr_set[dev] = true;
+    }
+    if (!router_encode_fn()) {
+        set_error_message("cuTensorMapEncodeTiled is not available from the driver");
+        return cudaErrorNotSupported;
+    }
+    const RouterTcPlan pl = router_tc_plan(s);
+    __nv_bfloat16 *wsplit = static_cast<__nv_bfloat16 *>(scratch);
+    float *partial = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
+                                               (((size_t)s.E * 3 * s.d * 2 + 255) & ~(size_t)255));
+    const int64_t n = (int64_t)s.E * s.d;
+    split_router_weight_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(
+        Wr, n, s.d, wsplit);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+    CUtensorMap mx, mw;
+    if (!make_map(&mx, x, s.T, s.d, RBM) || !make_map(&mw, wsplit, s.E, 3 * (int64_t)s.d, s.E)) {
+        set_error_message("cuTensorMapEncodeTiled rejected a router operand");
+        return cudaErrorInvalidValue;
+    }
+    RouterParams p;
+    p.partial = partial;
+    p.T = s.T;
+    p.d = s.d;
+    p.E = s.E;
+    p.ks_per_split = pl.ks_per_split;
+    p.ks_total = pl.ks_total;
+    p.idesc = idesc_bf16(RBM, s.E, false);
+    p.tmem_cols = s.E <= 32 ? 32 : s.E <= 64 ? 64 : s.E <= 128 ? 128 : 256;
+    p.ds = ds;
+    dim3 grid((unsigned)((s.T + RBM - 1) / RBM), (unsigned)pl.splits);
+    router_logits_tc_kernel<<<grid, R_THREADS, R_SMEM_BYTES, st>>>(mx, mw, p);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    *partial_out = partial;
+    *splits_out = pl.splits;
+    return cudaSuccess;
+}
+
+}  // namespace moe

@@ -55,7 +55,8 @@ def _load():
         "moe_last_error_message": ([], ctypes.c_char_p),
         "moe_workspace_size": ([cfgp], sz),
         "moe_dispatch_workspace_size": ([cfgp], sz),
-        "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp], st),
+        "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
+        "moe_route_workspace_size": ([cfgp], sz),
         "moe_route_from_logits": ([cfgp, vp, vp, vp, vp], st),
         "moe_dispatch": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "moe_grouped_swiglu": ([cfgp, vp, vp, vp, vp, vp, vp, vp], st),
@@ -141,9 +142,16 @@ def moe_debug_inject_wait_timeout(enable: bool) -> None:
     _lib.moe_debug_inject_wait_timeout(int(bool(enable)))
 
 
-def moe_route(cfg, x, Wr, logit_bias, logits, topk_idx, topk_w, stream=None, raise_on_error=True):
+def moe_route_workspace_size(cfg: moe_config_t) -> int:
+    return int(_lib.moe_route_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_route(cfg, x, Wr, logit_bias, logits, topk_idx, topk_w, ws=None, ws_bytes=None,
+              stream=None, raise_on_error=True):
+    if ws_bytes is None:
+        ws_bytes = 0 if ws is None or isinstance(ws, int) else ws.numel() * ws.element_size()
     s = _lib.moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wr), _ptr(logit_bias), _ptr(logits),
-                       _ptr(topk_idx), _ptr(topk_w), _stream(stream))
+                       _ptr(topk_idx), _ptr(topk_w), _ptr(ws), int(ws_bytes), _stream(stream))
     return _check(s, "moe_route", raise_on_error)
 
 
