@@ -17,7 +17,7 @@
 // the array and must be serialised by the caller.
 #include <mutex>
 
-#include "../../include/moe.h"
+#include "moe.h"
 #include "kernels.h"
 
 namespace {

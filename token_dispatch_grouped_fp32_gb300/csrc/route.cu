@@ -289,24 +289,35 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
 
     float v[VPL];
     unsigned avail = 0;  // bit i: value i of this lane is a not-yet-chosen expert
+    const float *src = nparts > 0 ? partial + t * E : L;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-        int e = lane + 32 * i;
-        if (e < E) {
-            if (nparts > 0) {
-                float a = partial[t * E + e];
-                for (int q = 1; q < nparts; ++q) a += partial[(int64_t)q * T * E + t * E + e];
-                if (bias) a += bias[e];
-                L[e] = a;
-                v[i] = a;
-            } else {
-                v[i] = L[e];
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? src[e] : 0.f;
+        if (e < E) avail |= 1u << i;
+    }
+    if (nparts > 0) {
+        // remaining partial buffers, each added to all VPL values at once
+        for (int q = 1; q < nparts; ++q) {
+            const float *pq = partial + (int64_t)q * T * E + t * E;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                const int e = lane + 32 * i;
+                if (e < E) v[i] += pq[e];
             }
-            avail |= 1u << i;
-        } else {
-            v[i] = -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                if (bias) v[i] += bias[e];
+                L[e] = v[i];
+            }
         }
     }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+        if (!((avail >> i) & 1u)) v[i] = -INFINITY;
 
     float my_v = 0.f;
     int my_e = 0;
