@@ -206,6 +206,7 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
     scatter_kernel<<<g.blocks, kThreads, sh, st>>>(idx, P, s.k, s.E, g.chunk, g.blocks, hist, pos,
                                                   src_token);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (!x_perm) return cudaSuccess;
     const int row_vecs = (int)((int64_t)s.d * (s.bf16 ? 2 : 4) / 16);
     const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
     gather_rows_kernel<<<blocks, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), pos, P, s.k,

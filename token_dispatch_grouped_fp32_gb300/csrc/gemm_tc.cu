@@ -226,14 +226,14 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                     ok = false;
                     break;
                 }
+                const uint32_t fb = sig_full + 8 * s;
+                const int k0 = ks * BK;
+                if (lane == 0 && leader) {
+                    mbar_arrive_expect_tx(bar_full + 8 * s, C::EXPECT_BYTES);
+                    issued |= 1u << s;
+                    last_par = (last_par & ~(1u << s)) | (ph << s);
+                }
                 if (lane == 0) {
-                    if (leader) {
-                        mbar_arrive_expect_tx(bar_full + 8 * s, C::EXPECT_BYTES);
-                        issued |= 1u << s;
-                        last_par = (last_par & ~(1u << s)) | (ph << s);
-                    }
-                    const uint32_t fb = sig_full + 8 * s;
-                    const int k0 = ks * BK;
                     tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, &tmA, k0, arow, fb);
                     const uint32_t bdst = base_s + C::OFF_B + s * C::B_BYTES;
 #pragma unroll
@@ -417,57 +417,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 }
 
 // ------------------------------ host side ----------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// Rows x cols bf16 matrix (cols contiguous), box 64 cols x 128 rows, 128 B swizzle.
-bool make_map_rows(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols) {
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)BM};
-    cuuint32_t estr[2] = {1, 1};
-    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
-                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// E x K x N bf16 weights (N contiguous), box 64 cols x 64 K-rows x 1 expert.
-bool make_map_weights(CUtensorMap *m, const void *ptr, int64_t E, int64_t K, int64_t N) {
-    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)K, (cuuint64_t)E};
-    cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)K * N * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)BK, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims,
-                       strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;    // single CTAs that fit at once (one per SM)
     int pairs = 0;  // CTA pairs that fit at once
 };
 
-template <bool SWIGLU, int CTAS>
+template <int CTAS>
 cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttribute *attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -487,7 +443,7 @@ template <bool SWIGLU, int CTAS>
 cudaError_t launch(unsigned grid, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p,
                    cudaStream_t st) {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config<SWIGLU, CTAS>(grid, st, attr);
+    cudaLaunchConfig_t cfg = launch_config<CTAS>(grid, st, attr);
     return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, CTAS>, ta, tb, p);
 }
 
@@ -497,8 +453,9 @@ template <bool SWIGLU, int CTAS> cudaError_t prepare(int *resident_units) {
                                            Cfg<CTAS>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config<SWIGLU, CTAS>(CTAS, nullptr, attr);
-    return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<SWIGLU, CTAS>, &cfg);
+    cudaLaunchConfig_t cfg = launch_config<CTAS>(CTAS, nullptr, attr);
+    return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<SWIGLU, CTAS>,
+                                          &cfg);
 }
 
 template <int CTAS>
@@ -560,14 +517,15 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
         }
         info[dev].ready = true;
     }
-    if (!encode_fn()) {
+    if (!tensor_map_encoder()) {
         set_error_message("cuTensorMapEncodeTiled is not available from the driver");
         return cudaErrorNotSupported;
     }
     const int64_t P = s.P();
     CUtensorMap mx, mwgu, mh, mwd;
-    if (!make_map_rows(&mx, x_perm, P, s.d) || !make_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) ||
-        !make_map_rows(&mh, h_perm, P, s.f) || !make_map_weights(&mwd, Wd, s.E, s.f, s.d)) {
+    if (!tensor_map_rows(&mx, x_perm, P, s.d, BM) ||
+        !tensor_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) ||
+        !tensor_map_rows(&mh, h_perm, P, s.f, BM) || !tensor_map_weights(&mwd, Wd, s.E, s.f, s.d)) {
         set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
         return cudaErrorInvalidValue;
     }

@@ -48,6 +48,7 @@ struct DispatchGrid {
 };
 DispatchGrid dispatch_grid(int64_t P);
 size_t dispatch_scratch_bytes(const Shape &s);  // per-block histogram ints
+// x_perm == nullptr: counts, offsets, pos and src_token only (no row gather).
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st);

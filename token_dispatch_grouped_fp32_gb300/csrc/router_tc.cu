@@ -205,38 +205,6 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     if (warp == 0) tmem_dealloc<1>(tmem, p.tmem_cols);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn router_encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// rows x cols bf16 (cols contiguous), box 64 cols x box_rows rows, 128 B swizzle
-bool make_map(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
-    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    cuuint32_t box[2] = {64, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return router_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims,
-                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 bool router_tc_eligible(const Shape &s) {
@@ -277,7 +245,7 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
             return err;
         attr_set[dev] = true;
     }
-    if (!router_encode_fn()) {
+    if (!tensor_map_encoder()) {
         set_error_message("cuTensorMapEncodeTiled is not available from the driver");
         return cudaErrorNotSupported;
     }
@@ -291,7 +259,8 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     CUtensorMap mx, mw;
-    if (!make_map(&mx, x, s.T, s.d, RBM) || !make_map(&mw, wsplit, s.E, 3 * (int64_t)s.d, s.E)) {
+    if (!tensor_map_rows(&mx, x, s.T, s.d, RBM) ||
+        !tensor_map_rows(&mw, wsplit, s.E, 3 * (int64_t)s.d, (uint32_t)s.E)) {
         set_error_message("cuTensorMapEncodeTiled rejected a router operand");
         return cudaErrorInvalidValue;
     }
