@@ -40,29 +40,80 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    i64, i32 = ctypes.c_int64, ctypes.c_int32
+    vp = ctypes.c_void_p
+    lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_router_logits.argtypes = [i64, i32, i32, vp, vp, vp, vp]
+    lib.oracle_topk.argtypes = [i64, i32, i32, i32, vp, vp, vp]
+    lib.oracle_dispatch.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
+    lib.oracle_expert_ffn_row.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_token_outputs.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_moe_forward.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+                                       vp, vp, vp, vp, vp, vp, vp, vp]
+    for fn in ("oracle_router_logits", "oracle_topk", "oracle_dispatch",
+               "oracle_expert_ffn_row", "oracle_token_outputs", "oracle_moe_forward"):
+        getattr(lib, fn).restype = None
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            i64, i32 = ctypes.c_int64, ctypes.c_int32
-            vp = ctypes.c_void_p
-            lib.oracle_num_threads.restype = ctypes.c_int
-            lib.oracle_router_logits.argtypes = [i64, i32, i32, vp, vp, vp, vp]
-            lib.oracle_topk.argtypes = [i64, i32, i32, i32, vp, vp, vp]
-            lib.oracle_dispatch.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
-            lib.oracle_expert_ffn_row.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
-            lib.oracle_token_outputs.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp,
-                                                 vp, vp, vp]
-            lib.oracle_moe_forward.argtypes = [i64, i32, i32, i32, i32, i32,
-                                               vp, vp, vp, vp, vp,
-                                               vp, vp, vp, vp, vp, vp, vp, vp]
-            for fn in ("oracle_router_logits", "oracle_topk", "oracle_dispatch",
-                       "oracle_expert_ffn_row", "oracle_token_outputs",
-                       "oracle_moe_forward"):
-                getattr(lib, fn).restype = None
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def build_from_source(source: str, tag: str) -> str:
+    """Compile a (test-modified) copy of the oracle source; returns the .so path.
+    Used only by the mutation test, which plants mistakes in the oracle."""
+    d = os.path.join(_BUILD_DIR, "variants")
+    os.makedirs(d, exist_ok=True)
+    src = os.path.join(d, f"{tag}.c")
+    out = os.path.join(d, f"lib{tag}.so")
+    with open(src, "w") as fh:
+        fh.write(source)
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                    "-fno-fast-math", src, "-o", out, "-lm"], check=True)
+    return out
+
+
+def source() -> str:
+    with open(_SRC) as fh:
+        return fh.read()
+
+
+class Oracle:
+    """The functions below, bound to a given oracle library (for the
+    mutation test); the module-level functions use the built-in library."""
+
+    def __init__(self, lib_path: str):
+        self._lib = _bind(ctypes.CDLL(lib_path))
+
+    def _use(self):
+        return _Scoped(self._lib)
+
+
+class _Scoped:
+    def __init__(self, lib):
+        self.lib = lib
+
+    def __enter__(self):
+        global _lib_override
+        self.prev = _lib_override
+        _lib_override = self.lib
+
+    def __exit__(self, *exc):
+        global _lib_override
+        _lib_override = self.prev
+
+
+_lib_override = None
+
+
+def _L():
+    return _lib_override if _lib_override is not None else _load()
 
 
 def _f32(a):
@@ -78,7 +129,7 @@ def _p(a):
 
 
 def num_threads() -> int:
-    return int(_load().oracle_num_threads())
+    return int(_L().oracle_num_threads())
 
 
 def router_logits(x, Wr, bias=None):
@@ -88,7 +139,7 @@ def router_logits(x, Wr, bias=None):
     E = Wr.shape[0]
     b = None if bias is None else _f32(bias)
     out = np.empty((T, E), np.float32)
-    _load().oracle_router_logits(T, d, E, _p(x), _p(Wr), _p(b), _p(out))
+    _L().oracle_router_logits(T, d, E, _p(x), _p(Wr), _p(b), _p(out))
     return out
 
 
@@ -98,7 +149,7 @@ def topk(logits, k, renorm=True):
     T, E = L.shape
     idx = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
-    _load().oracle_topk(T, E, k, int(bool(renorm)), _p(L), _p(idx), _p(w))
+    _L().oracle_topk(T, E, k, int(bool(renorm)), _p(L), _p(idx), _p(w))
     return idx, w
 
 
@@ -111,7 +162,7 @@ def dispatch(idx, E):
     offsets = np.empty(E + 1, np.int32)
     pos = np.empty(P, np.int32)
     src = np.empty(P, np.int32)
-    _load().oracle_dispatch(T, E, k, _p(idx), _p(counts), _p(offsets), _p(pos), _p(src))
+    _L().oracle_dispatch(T, E, k, _p(idx), _p(counts), _p(offsets), _p(pos), _p(src))
     return counts, offsets, pos, src
 
 
@@ -123,7 +174,7 @@ def expert_ffn_row(xrow, Wgu_e, Wd_e):
     gu = np.empty(2 * f, np.float64)
     h = np.empty(f, np.float64)
     y = np.empty(d, np.float64)
-    _load().oracle_expert_ffn_row(d, f, _p(xrow), _p(Wgu_e), _p(Wd_e), _p(gu), _p(h), _p(y))
+    _L().oracle_expert_ffn_row(d, f, _p(xrow), _p(Wgu_e), _p(Wd_e), _p(gu), _p(h), _p(y))
     return h, y
 
 
@@ -136,7 +187,7 @@ def token_outputs(tokens, x, Wgu, Wd, idx, w):
     k = idx.shape[1]
     f = Wd.shape[1]
     out = np.empty((tokens.shape[0], d), np.float64)
-    _load().oracle_token_outputs(tokens.shape[0], _p(tokens), d, k, f, _p(x), _p(Wgu),
+    _L().oracle_token_outputs(tokens.shape[0], _p(tokens), d, k, f, _p(x), _p(Wgu),
                                  _p(Wd), _p(idx), _p(w), _p(out))
     return out
 
@@ -160,8 +211,22 @@ def moe_forward(x, Wr, Wgu, Wd, k, renorm=True, bias=None):
         "src_token": np.empty(P, np.int32),
         "out": np.empty((T, d), np.float64),
     }
-    _load().oracle_moe_forward(T, d, E, k, f, int(bool(renorm)), _p(x), _p(Wr), _p(b),
+    _L().oracle_moe_forward(T, d, E, k, f, int(bool(renorm)), _p(x), _p(Wr), _p(b),
                                _p(Wgu), _p(Wd), _p(r["logits"]), _p(r["idx"]), _p(r["w"]),
                                _p(r["counts"]), _p(r["offsets"]), _p(r["pos"]),
                                _p(r["src_token"]), _p(r["out"]))
     return r
+
+
+def _method(fn):
+    def m(self, *a, **k):
+        with self._use():
+            return fn(*a, **k)
+    m.__name__ = fn.__name__
+    m.__doc__ = fn.__doc__
+    return m
+
+
+for _fn in (num_threads, router_logits, topk, dispatch, expert_ffn_row, token_outputs,
+            moe_forward):
+    setattr(Oracle, _fn.__name__, _method(_fn))
