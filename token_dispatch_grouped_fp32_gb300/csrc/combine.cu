@@ -31,21 +31,36 @@ combine_kernel(const TA *__restrict__ y_perm, const int32_t *__restrict__ pos,
     }
     __syncwarp();
     const int nvec = d / EPV;
-    for (int v = lane; v < nvec; v += 32) {
-        float acc[EPV];
+    constexpr int U = 4;  // 16-byte vectors per lane in flight per slot
+    for (int v0 = lane; v0 < nvec; v0 += 32 * U) {
+        float acc[U][EPV];
 #pragma unroll
-        for (int i = 0; i < EPV; ++i) acc[i] = 0.f;
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int i = 0; i < EPV; ++i) acc[u][i] = 0.f;
         for (int j = 0; j < k; ++j) {
             const int row = s_pos[wid][j];
             if (row < 0) continue;  // dropped pair
             const float wj = s_w[wid][j];
-            float y[EPV];
-            unpack16(ldg16(y_perm + (int64_t)row * d + (int64_t)v * EPV), y,
-                     static_cast<const TA *>(nullptr));
+            const TA *yrow = y_perm + (int64_t)row * d;
+            uint4 raw[U];
 #pragma unroll
-            for (int i = 0; i < EPV; ++i) acc[i] = fmaf(wj, y[i], acc[i]);
+            for (int u = 0; u < U; ++u)
+                if (v0 + 32 * u < nvec) raw[u] = ldg16(yrow + (int64_t)(v0 + 32 * u) * EPV);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (v0 + 32 * u >= nvec) continue;
+                float y[EPV];
+                unpack16(raw[u], y, static_cast<const TA *>(nullptr));
+#pragma unroll
+                for (int i = 0; i < EPV; ++i) acc[u][i] = fmaf(wj, y[i], acc[u][i]);
+            }
         }
-        stg16(out + t * d + (int64_t)v * EPV, pack16(acc, static_cast<const TA *>(nullptr)));
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v0 + 32 * u < nvec)
+                stg16(out + t * d + (int64_t)(v0 + 32 * u) * EPV,
+                      pack16(acc[u], static_cast<const TA *>(nullptr)));
     }
 }
 

@@ -16,9 +16,13 @@ struct Shape {
     int64_t P() const { return T * (int64_t)k; }
 };
 
-// Router: logits[T][E] = x @ Wr^T (+ bias), fp32 accumulation.
+// Router: logits[T][E] = x @ Wr^T (+ bias), fp32 accumulation.  When
+// router_selects_in_logits(s) and idx/w are given, the same launch also
+// writes the top-k selection and weights (no separate top-k launch).
 cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr,
-                                 const float *bias, float *logits, cudaStream_t st);
+                                 const float *bias, float *logits, cudaStream_t st,
+                                 int32_t *idx = nullptr, float *w = nullptr);
+bool router_selects_in_logits(const Shape &s);
 // Top-k selection and softmax weights on a given fp32 logit buffer.
 cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
                         cudaStream_t st);

@@ -186,6 +186,9 @@ moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const flo
         return from_cuda(launch_topk_partials(s, partial, splits, bias, logits, idx, w, st),
                          "top-k launch");
     }
+    if (router_selects_in_logits(s))  // one launch: logits, selection and weights
+        return from_cuda(launch_router_logits(s, x, Wr, bias, logits, st, idx, w),
+                         "router launch");
     moe_status_t r = from_cuda(launch_router_logits(s, x, Wr, bias, logits, st),
                                "router logits launch");
     if (r != MOE_OK) return r;

@@ -57,11 +57,22 @@ __device__ __forceinline__ void warp_reduce_scatter32(float (&v)[32]) {
 
 constexpr int kSplitWarps = 8;
 
+// Rank order of the selection: a larger logit first; equal logits (+0.0 and
+// -0.0 are equal) to the lower expert id; a NaN below every number.
+__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
+    const bool an = isnan(a), bn = isnan(b);
+    if (an || bn) return (an && bn) ? (ia < ib) : bn;
+    if (a > b) return true;
+    if (a < b) return false;
+    return ia < ib;
+}
+
 template <typename TA, int EP>
 __global__ void __launch_bounds__(256)
 router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
                            const float *__restrict__ bias, float *__restrict__ logits,
-                           int64_t T, int d, int E) {
+                           int64_t T, int d, int E, int k, int renorm,
+                           int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
     constexpr int TPW = 32 / EP;
     __shared__ float red[kSplitWarps][32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -124,7 +135,51 @@ router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ W
         for (int w = 1; w < kSplitWarps; ++w) v += red[w][lane];
         const int tt = lane / EP, e = lane % EP;
         const int64_t t = t0 + tt;
-        if (e < ne && t < T) logits[t * E + e0 + e] = v + (bias ? bias[e0 + e] : 0.f);
+        v += bias ? bias[e0 + min(e, ne - 1)] : 0.f;
+        if (e < ne && t < T) logits[t * E + e0 + e] = v;
+        // E <= 32: select and weigh here, on exactly the values just written.
+        // Token tt's logits sit in the EP-lane segment of lanes tt*EP + e.
+        if (topk_idx != nullptr) {  // warp-uniform: every lane joins the shuffles
+            const bool valid = e < ne;
+            bool avail = valid;
+            float my_v = 0.f;
+            int my_e = 0;
+            for (int j = 0; j < k; ++j) {
+                float bv = avail ? v : NAN;
+                int be = avail ? e : 0x7fffffff;
+#pragma unroll
+                for (int off = EP / 2; off > 0; off >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+                    if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
+                        bv = ov;
+                        be = oe;
+                    }
+                }
+                if (be == e) avail = false;
+                if (e == j) {
+                    my_v = bv;
+                    my_e = be;
+                }
+            }
+            float m = valid ? v : -INFINITY;
+#pragma unroll
+            for (int off = EP / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            float z = valid ? expf(v - m) : 0.f;
+#pragma unroll
+            for (int off = EP / 2; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+            float pr = (e < k) ? expf(my_v - m) / z : 0.f;
+            if (renorm) {
+                float sum = pr;
+#pragma unroll
+                for (int off = EP / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                pr = pr / sum;
+            }
+            if (e < k && t < T) {
+                topk_idx[t * k + e] = my_e;
+                topk_w[t * k + e] = pr;
+            }
+        }
     }
 }
 
@@ -235,25 +290,30 @@ cudaError_t launch_logits_cfg(const Shape &s, const TA *x, const float *Wr, cons
 
 template <typename TA, int EP>
 cudaError_t launch_logits_split(const Shape &s, const TA *x, const float *Wr, const float *bias,
-                                float *logits, cudaStream_t st) {
+                                float *logits, int32_t *idx, float *w, cudaStream_t st) {
     constexpr int TPW = 32 / EP;
     dim3 grid((unsigned)((s.T + TPW - 1) / TPW), (unsigned)((s.E + EP - 1) / EP));
-    router_logits_split_kernel<TA, EP><<<grid, 256, 0, st>>>(x, Wr, bias, logits, s.T, s.d, s.E);
+    // with a single expert group (E <= 32) the kernel also selects; larger E
+    // leaves the selection to the top-k kernel
+    const bool fused = grid.y == 1 && idx != nullptr;
+    router_logits_split_kernel<TA, EP><<<grid, 256, 0, st>>>(
+        x, Wr, bias, logits, s.T, s.d, s.E, s.k, s.renorm ? 1 : 0, fused ? idx : nullptr,
+        fused ? w : nullptr);
     return cudaGetLastError();
 }
 
 template <typename TA>
 cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const float *bias,
-                            float *logits, cudaStream_t st) {
-    if (s.E <= 1) return launch_logits_split<TA, 1>(s, x, Wr, bias, logits, st);
-    if (s.E <= 2) return launch_logits_split<TA, 2>(s, x, Wr, bias, logits, st);
-    if (s.E <= 4) return launch_logits_split<TA, 4>(s, x, Wr, bias, logits, st);
-    if (s.E <= 8) return launch_logits_split<TA, 8>(s, x, Wr, bias, logits, st);
-    if (s.E <= 16) return launch_logits_split<TA, 16>(s, x, Wr, bias, logits, st);
-    if (s.E <= 32) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, st);
+                            float *logits, int32_t *idx, float *w, cudaStream_t st) {
+    if (s.E <= 1) return launch_logits_split<TA, 1>(s, x, Wr, bias, logits, idx, w, st);
+    if (s.E <= 2) return launch_logits_split<TA, 2>(s, x, Wr, bias, logits, idx, w, st);
+    if (s.E <= 4) return launch_logits_split<TA, 4>(s, x, Wr, bias, logits, idx, w, st);
+    if (s.E <= 8) return launch_logits_split<TA, 8>(s, x, Wr, bias, logits, idx, w, st);
+    if (s.E <= 16) return launch_logits_split<TA, 16>(s, x, Wr, bias, logits, idx, w, st);
+    if (s.E <= 32) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, idx, w, st);
     // larger E: the tiled kernel re-reads Wr far less per token, but needs
     // enough row tiles to fill the GPU; small batches use 32-expert groups.
-    if (s.T < 2048) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, st);
+    if (s.T < 2048) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, idx, w, st);
     if (s.E <= 64) return launch_logits_cfg<TA, 64, 64, 4, 4>(s, x, Wr, bias, logits, st);
     return launch_logits_cfg<TA, 64, 128, 4, 8>(s, x, Wr, bias, logits, st);
 }
@@ -264,13 +324,6 @@ cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const 
 // lane j.  Weights: softmax over all E logits (max-shifted), then optional
 // renormalisation over the chosen k.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
-    const bool an = isnan(a), bn = isnan(b);
-    if (an || bn) return (an && bn) ? (ia < ib) : bn;
-    if (a > b) return true;
-    if (a < b) return false;
-    return ia < ib;
-}
 
 constexpr int kNoExpert = 0x7fffffff;
 
@@ -396,12 +449,14 @@ cudaError_t launch_topk_any(const Shape &s, float *logits, const float *partial,
 }  // namespace
 
 cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr, const float *bias,
-                                 float *logits, cudaStream_t st) {
+                                 float *logits, cudaStream_t st, int32_t *idx, float *w) {
     if (s.bf16)
         return launch_logits_t<__nv_bfloat16>(s, static_cast<const __nv_bfloat16 *>(x), Wr, bias,
-                                              logits, st);
-    return launch_logits_t<float>(s, static_cast<const float *>(x), Wr, bias, logits, st);
+                                              logits, idx, w, st);
+    return launch_logits_t<float>(s, static_cast<const float *>(x), Wr, bias, logits, idx, w, st);
 }
+
+bool router_selects_in_logits(const Shape &s) { return s.E <= 32; }
 
 cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
                         cudaStream_t st) {
