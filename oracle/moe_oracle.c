@@ -182,22 +182,24 @@ void oracle_dispatch(int64_t T, int32_t E, int32_t k, const int32_t *idx,
 }
 
 /*
- * One expert's SwiGLU FFN on one row [TP-pack, EP-add]:
- *   gu   = x @ Wgu_e            (Wgu_e is d x 2f, row-major)
+ * One expert's SwiGLU FFN on one row [TP-pack, EP-add], on the input row
+ * scaled by `scale` (1 unless the routing weights scale expert inputs):
+ *   gu   = (scale * x) @ Wgu_e  (Wgu_e is d x 2f, row-major)
  *   gate = gu[0:f], up = gu[f:2f]          (chunk(2, dim=-1))
  *   h    = silu(gate) * up,  silu(z) = z / (1 + exp(-z))
  *   y    = h @ Wd_e             (Wd_e is f x d, row-major)
  * gu (2f) and h (f) are caller scratch; y has d entries.
  */
-void oracle_expert_ffn_row(int32_t d, int32_t f, const float *xrow,
-                           const float *Wgu_e, const float *Wd_e, double *gu,
-                           double *h, double *y)
+static void expert_ffn_row_scaled(int32_t d, int32_t f, const float *xrow,
+                                  double scale, const float *Wgu_e,
+                                  const float *Wd_e, double *gu, double *h,
+                                  double *y)
 {
     int64_t two_f = 2 * (int64_t)f;
     for (int64_t c = 0; c < two_f; ++c)
         gu[c] = 0.0;
     for (int32_t i = 0; i < d; ++i) {
-        double xi = (double)xrow[i];
+        double xi = scale * (double)xrow[i];
         const float *wrow = Wgu_e + (int64_t)i * two_f;
         for (int64_t c = 0; c < two_f; ++c)
             gu[c] += xi * (double)wrow[c];
@@ -216,17 +218,28 @@ void oracle_expert_ffn_row(int32_t d, int32_t f, const float *xrow,
     }
 }
 
+void oracle_expert_ffn_row(int32_t d, int32_t f, const float *xrow,
+                           const float *Wgu_e, const float *Wd_e, double *gu,
+                           double *h, double *y)
+{
+    expert_ffn_row_scaled(d, f, xrow, 1.0, Wgu_e, Wd_e, gu, h, y);
+}
+
 /*
  * Layer output of selected tokens [EP-add, EP-disp]: for each listed token t,
  * out[n] = sum over slots j = 0..k-1, in slot order, of
- * w[t][j] * FFN_{idx[t][j]}(x[t]).  Each (t, j) pair's expert row is exactly
- * the row the dispatch would send, so this is the combine written per token.
- * out is [ntok][d].
+ *   w[t][j] * FFN_{idx[t][j]}(x[t])        (scale_inputs == 0), or
+ *   FFN_{idx[t][j]}(w[t][j] * x[t])        (scale_inputs != 0: the experts
+ *                                            receive tokens already scaled
+ *                                            by the router score [EP intro]).
+ * Each (t, j) pair's expert row is exactly the row the dispatch would send,
+ * so this is the combine written per token.  out is [ntok][d].
  */
 void oracle_token_outputs(int64_t ntok, const int64_t *tokens, int32_t d,
                           int32_t k, int32_t f, const float *x,
                           const float *Wgu, const float *Wd,
-                          const int32_t *idx, const double *w, double *out)
+                          const int32_t *idx, const double *w,
+                          int32_t scale_inputs, double *out)
 {
     int64_t n;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -240,9 +253,12 @@ void oracle_token_outputs(int64_t ntok, const int64_t *tokens, int32_t d,
             o[c] = 0.0;
         for (int32_t j = 0; j < k; ++j) {
             int64_t e = idx[t * k + j];
-            oracle_expert_ffn_row(d, f, x + t * d, Wgu + e * (int64_t)d * 2 * f,
-                                  Wd + e * (int64_t)f * d, gu, h, y);
             double wj = w[t * k + j];
+            expert_ffn_row_scaled(d, f, x + t * d, scale_inputs ? wj : 1.0,
+                                  Wgu + e * (int64_t)d * 2 * f,
+                                  Wd + e * (int64_t)f * d, gu, h, y);
+            if (scale_inputs)
+                wj = 1.0;
             for (int32_t c = 0; c < d; ++c)
                 o[c] += wj * y[c];
         }
@@ -255,27 +271,34 @@ void oracle_token_outputs(int64_t ntok, const int64_t *tokens, int32_t d,
 /*
  * Whole layer, in the method's order [EP-disp]: logits, top-k, dispatch,
  * each expert on the rows sent to it (y_perm, row by row), then the combine
- * out[t] = sum_j w[t][j] * y_perm[pos[t][j]] in slot order.
+ * out[t] = sum_j w[t][j] * y_perm[pos[t][j]] in slot order.  With
+ * scale_inputs the weight scales each expert's input row instead and the
+ * combine sums the rows unweighted [EP intro: experts that receive tokens
+ * already scaled by the router score].
  * Outputs: logits [T][E], idx/w [T][k], counts [E], offsets [E+1],
  * pos [T*k], src_token [T*k], out [T][d].
  */
 void oracle_moe_forward(int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
-                        int32_t renorm, const float *x, const float *Wr,
-                        const float *bias, const float *Wgu, const float *Wd,
-                        float *logits, int32_t *idx, double *w,
-                        int32_t *counts, int32_t *offsets, int32_t *pos,
-                        int32_t *src_token, double *out)
+                        int32_t renorm, int32_t scale_inputs, const float *x,
+                        const float *Wr, const float *bias, const float *Wgu,
+                        const float *Wd, float *logits, int32_t *idx,
+                        double *w, int32_t *counts, int32_t *offsets,
+                        int32_t *pos, int32_t *src_token, double *out)
 {
     int64_t P = T * k;
     oracle_router_logits(T, d, E, x, Wr, bias, logits);
     oracle_topk(T, E, k, renorm, logits, idx, w);
     oracle_dispatch(T, E, k, idx, counts, offsets, pos, src_token);
 
-    /* Expert id of each dispatched row: the e whose segment holds it. */
+    /* Expert id of each dispatched row: the e whose segment holds it, and the
+     * routing weight the row carries (scale_inputs: applied to the input). */
     int32_t *row_expert = (int32_t *)malloc(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+    double *row_scale = (double *)malloc(sizeof(double) * (size_t)(P > 0 ? P : 1));
     for (int32_t e = 0; e < E; ++e)
         for (int32_t r = offsets[e]; r < offsets[e + 1]; ++r)
             row_expert[r] = e;
+    for (int64_t q = 0; q < P; ++q)
+        row_scale[pos[q]] = scale_inputs ? w[q] : 1.0;
 
     double *y_perm = (double *)malloc(sizeof(double) * (size_t)(P > 0 ? P : 1) * (size_t)d);
     int64_t r;
@@ -285,7 +308,8 @@ void oracle_moe_forward(int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
         int64_t t = src_token[r];
         double *gu = (double *)malloc(sizeof(double) * 2 * (size_t)f);
         double *h = (double *)malloc(sizeof(double) * (size_t)f);
-        oracle_expert_ffn_row(d, f, x + t * d, Wgu + e * (int64_t)d * 2 * f,
+        expert_ffn_row_scaled(d, f, x + t * d, row_scale[r],
+                              Wgu + e * (int64_t)d * 2 * f,
                               Wd + e * (int64_t)f * d, gu, h, y_perm + r * d);
         free(gu);
         free(h);
@@ -299,11 +323,12 @@ void oracle_moe_forward(int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
             o[c] = 0.0;
         for (int32_t j = 0; j < k; ++j) {
             const double *yr = y_perm + (int64_t)pos[t * k + j] * d;
-            double wj = w[t * k + j];
+            double wj = scale_inputs ? 1.0 : w[t * k + j];
             for (int32_t c = 0; c < d; ++c)
                 o[c] += wj * yr[c];
         }
     }
     free(y_perm);
     free(row_expert);
+    free(row_scale);
 }

@@ -48,8 +48,8 @@ def _bind(lib):
     lib.oracle_topk.argtypes = [i64, i32, i32, i32, vp, vp, vp]
     lib.oracle_dispatch.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
     lib.oracle_expert_ffn_row.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
-    lib.oracle_token_outputs.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, vp]
-    lib.oracle_moe_forward.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
+    lib.oracle_token_outputs.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]
+    lib.oracle_moe_forward.argtypes = [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                        vp, vp, vp, vp, vp, vp, vp, vp]
     for fn in ("oracle_router_logits", "oracle_topk", "oracle_dispatch",
                "oracle_expert_ffn_row", "oracle_token_outputs", "oracle_moe_forward"):
@@ -178,8 +178,10 @@ def expert_ffn_row(xrow, Wgu_e, Wd_e):
     return h, y
 
 
-def token_outputs(tokens, x, Wgu, Wd, idx, w):
-    """Layer output rows [len(tokens), d] (float64) for the listed tokens."""
+def token_outputs(tokens, x, Wgu, Wd, idx, w, scale_inputs=False):
+    """Layer output rows [len(tokens), d] (float64) for the listed tokens.
+    scale_inputs: the routing weights scale each expert's input instead of
+    its output."""
     x, Wgu, Wd, idx = _f32(x), _f32(Wgu), _f32(Wd), _i32(idx)
     w = np.ascontiguousarray(w, dtype=np.float64)
     tokens = np.ascontiguousarray(tokens, dtype=np.int64)
@@ -188,13 +190,14 @@ def token_outputs(tokens, x, Wgu, Wd, idx, w):
     f = Wd.shape[1]
     out = np.empty((tokens.shape[0], d), np.float64)
     _L().oracle_token_outputs(tokens.shape[0], _p(tokens), d, k, f, _p(x), _p(Wgu),
-                                 _p(Wd), _p(idx), _p(w), _p(out))
+                              _p(Wd), _p(idx), _p(w), int(bool(scale_inputs)), _p(out))
     return out
 
 
-def moe_forward(x, Wr, Wgu, Wd, k, renorm=True, bias=None):
+def moe_forward(x, Wr, Wgu, Wd, k, renorm=True, bias=None, scale_inputs=False):
     """Whole layer.  Returns a dict with logits, idx, w, counts, offsets, pos,
-    src_token and out (float64 [T, d])."""
+    src_token and out (float64 [T, d]).  scale_inputs: the routing weights
+    scale each expert's input instead of its output."""
     x, Wr, Wgu, Wd = _f32(x), _f32(Wr), _f32(Wgu), _f32(Wd)
     T, d = x.shape
     E = Wr.shape[0]
@@ -211,7 +214,8 @@ def moe_forward(x, Wr, Wgu, Wd, k, renorm=True, bias=None):
         "src_token": np.empty(P, np.int32),
         "out": np.empty((T, d), np.float64),
     }
-    _L().oracle_moe_forward(T, d, E, k, f, int(bool(renorm)), _p(x), _p(Wr), _p(b),
+    _L().oracle_moe_forward(T, d, E, k, f, int(bool(renorm)), int(bool(scale_inputs)), _p(x),
+                            _p(Wr), _p(b),
                                _p(Wgu), _p(Wd), _p(r["logits"]), _p(r["idx"]), _p(r["w"]),
                                _p(r["counts"]), _p(r["offsets"]), _p(r["pos"]),
                                _p(r["src_token"]), _p(r["out"]))

@@ -26,6 +26,9 @@ CHECKS = [
     ("brute_force", lambda o: pins.test_brute_force_tiny_layer(o, False)),
     ("brute_force_bias", lambda o: pins.test_brute_force_tiny_layer(o, True)),
     ("token_outputs_rows", lambda o: pins.test_token_outputs_equal_forward_rows(o)),
+    ("input_scaled_dense", lambda o: pins.test_input_scaled_equals_dense_no_dispatch(o, 6, 2, True)),
+    ("input_scaled_kE", lambda o: pins.test_input_scaled_equals_dense_no_dispatch(o, 6, 6, False)),
+    ("input_scaled_one_expert", lambda o: pins.test_input_scaled_single_expert_is_plain_mlp(o)),
 ]
 
 if __name__ == "__main__":

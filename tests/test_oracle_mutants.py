@@ -26,10 +26,14 @@ MUTANTS = {
                                  "        for (int32_t j = 0; j < k; ++j)\n            Z += exp((double)L[idx[t * k + j]] - m);"),
     "dispatch_reverse_tokens": ("    for (int64_t t = 0; t < T; ++t) {\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx[t * k + j];",
                                 "    for (int64_t t = T - 1; t >= 0; --t) {\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx[t * k + j];"),
-    "combine_wrong_slot_weight": ("            double wj = w[t * k + j];\n            for (int32_t c = 0; c < d; ++c)\n                o[c] += wj * y[c];",
-                                  "            double wj = w[t * k + (k - 1 - j)];\n            for (int32_t c = 0; c < d; ++c)\n                o[c] += wj * y[c];"),
-    "forward_combine_wrong_slot": ("            const double *yr = y_perm + (int64_t)pos[t * k + j] * d;\n            double wj = w[t * k + j];",
-                                   "            const double *yr = y_perm + (int64_t)pos[t * k + j] * d;\n            double wj = w[t * k + (k - 1 - j)];"),
+    "combine_wrong_slot_weight": ("            int64_t e = idx[t * k + j];\n            double wj = w[t * k + j];",
+                                  "            int64_t e = idx[t * k + j];\n            double wj = w[t * k + (k - 1 - j)];"),
+    "forward_combine_wrong_slot": ("            double wj = scale_inputs ? 1.0 : w[t * k + j];",
+                                   "            double wj = scale_inputs ? 1.0 : w[t * k + (k - 1 - j)];"),
+    "input_scale_also_on_output": ("            double wj = scale_inputs ? 1.0 : w[t * k + j];",
+                                   "            double wj = w[t * k + j];"),
+    "input_scale_ignored": ("        row_scale[pos[q]] = scale_inputs ? w[q] : 1.0;",
+                            "        row_scale[pos[q]] = 1.0;"),
     "bias_dropped": ("            if (bias)\n                s += (double)bias[e];", "            (void)bias;"),
     "router_weight_transposed": ("s += (double)x[t * d + i] * (double)Wr[(int64_t)e * d + i];",
                                  "s += (double)x[t * d + i] * (double)Wr[(int64_t)i * E + e];"),

@@ -202,3 +202,39 @@ def test_empty_batch(oracle):
     r = oracle.moe_forward(x, Wr, Wgu, Wd, w.k)
     assert r["out"].shape == (0, w.d)
     assert (r["counts"] == 0).all() and (r["offsets"] == 0).all()
+
+
+@pytest.mark.parametrize("E,k,renorm", [(6, 2, True), (6, 6, False), (4, 1, True)])
+def test_input_scaled_equals_dense_no_dispatch(oracle, E, k, renorm):
+    """Routing weights on the expert inputs: the layer equals the form with
+    nothing to dispatch, in which every expert receives every token already
+    scaled by its router score (0 for experts the token did not pick, and
+    SwiGLU(0) = 0 without biases).  Computed here densely with matmuls."""
+    w = synth.Workload("in", 23, 40, E, k, 24, "f32", 31)
+    inp = synth.make_inputs(w)
+    x, Wr, Wgu, Wd = (inp[n].numpy() for n in ("x", "Wr", "Wgu", "Wd"))
+    r = oracle.moe_forward(x, Wr, Wgu, Wd, k, renorm=renorm, scale_inputs=True)
+    s = np.zeros((w.T, E))
+    np.put_along_axis(s, r["idx"].astype(np.int64), r["w"], axis=1)
+    dense = sum(_np_expert(s[:, e:e + 1] * x.astype(np.float64), Wgu[e], Wd[e]) for e in range(E))
+    np.testing.assert_allclose(r["out"], dense, rtol=1e-9, atol=1e-12)
+    # and the weights really do act on the inputs: unless every weight is 1
+    # (k = 1 renormalised), the output-weighted layer differs
+    r_out = oracle.moe_forward(x, Wr, Wgu, Wd, k, renorm=renorm, scale_inputs=False)
+    if np.all(r["w"] == 1.0):
+        np.testing.assert_array_equal(r_out["out"], r["out"])
+    else:
+        assert np.abs(r_out["out"] - r["out"]).max() > 1e-3
+
+
+def test_input_scaled_single_expert_is_plain_mlp(oracle):
+    w = synth.Workload("in1", 17, 32, 1, 1, 16, "f32", 32)
+    inp = synth.make_inputs(w)
+    x, Wr, Wgu, Wd = (inp[n].numpy() for n in ("x", "Wr", "Wgu", "Wd"))
+    a = oracle.moe_forward(x, Wr, Wgu, Wd, 1, scale_inputs=True)["out"]
+    b = oracle.moe_forward(x, Wr, Wgu, Wd, 1, scale_inputs=False)["out"]
+    np.testing.assert_array_equal(a, b)
+    toks = np.array([0, 3, 16])
+    c = oracle.token_outputs(toks, x, Wgu, Wd, np.zeros((17, 1), np.int32), np.ones((17, 1)),
+                             scale_inputs=True)
+    np.testing.assert_array_equal(c, a[toks])
