@@ -315,7 +315,7 @@ def run_ours(args, w):
         if ev: ev[0].record(stream)
         moe.moe_route(cfg, x, Wr, bias, logits, idx, wt, rws, stream=stream)
         if ev: ev[1].record(stream)
-        moe.moe_dispatch(cfg, idx, x, counts, offsets, pos, src, x_perm, dws, stream=stream)
+        moe.moe_dispatch(cfg, idx, wt, x, counts, offsets, pos, src, x_perm, dws, stream=stream)
         if ev: ev[2].record(stream)
         moe.moe_grouped_swiglu(cfg, x_perm, offsets, Wgu, Wd, h_perm, y_perm, stream=stream)
         if ev: ev[3].record(stream)

@@ -75,6 +75,11 @@ typedef struct {
     int32_t f;           /* expert FFN width (gate and up each have f columns) */
     int32_t act_dtype;   /* moe_dtype_t */
     int32_t renormalize; /* 1: divide the chosen k softmax weights by their sum; 0: keep them */
+    int32_t scale_inputs;  /* 0: routing weights scale the expert outputs in the combine;
+                              1: they scale the expert inputs in the dispatch and the
+                              combine sums unweighted (experts that receive tokens already
+                              scaled by the router score [EP]; with k == E every expert
+                              sees every token: the form with nothing to dispatch) */
 } moe_config_t;
 
 /* Human-readable name of a status.  Never NULL; the string is static. */
@@ -145,14 +150,17 @@ moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits,
  *                   rows of one expert are in ascending token order)    [P]
  *   src_token[r]  = token of row r (src_token[pos[q]] == q / k)         [P]
  *   x_perm[r][:]  = x[src_token[r]][:]                                  [P][d] act dtype
+ *                   (scale_inputs: topk_w[q] * x[t][:], formed in fp32 and
+ *                   rounded once to the act dtype, for the pair q of row r)
  * topk_idx is [T][k] int32; each entry must lie in [0, E) -- an entry outside
  * sets MOE_ERR_BAD_ROUTING in the device error word and that pair is dropped.
+ * topk_w [T][k] fp32: read only when cfg->scale_inputs (may be NULL otherwise).
  * ws: at least moe_dispatch_workspace_size(cfg) bytes, 256-byte aligned.
  */
 moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
-                          const void *x, int32_t *counts, int32_t *offsets,
-                          int32_t *pos, int32_t *src_token, void *x_perm,
-                          void *ws, size_t ws_bytes, void *stream);
+                          const float *topk_w, const void *x, int32_t *counts,
+                          int32_t *offsets, int32_t *pos, int32_t *src_token,
+                          void *x_perm, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * moe_dispatch without a caller workspace.  (The pages have no counterpart:
@@ -177,9 +185,9 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
  * Other arguments, errors and outputs are as for moe_dispatch.
  */
 moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int32_t *topk_idx,
-                                  const void *x, int32_t *counts, int32_t *offsets,
-                                  int32_t *pos, int32_t *src_token, void *x_perm,
-                                  void *stream);
+                                  const float *topk_w, const void *x, int32_t *counts,
+                                  int32_t *offsets, int32_t *pos, int32_t *src_token,
+                                  void *x_perm, void *stream);
 
 /*
  * Grouped SwiGLU experts [EP-add: experts_forward; TP-pack]: for every expert
@@ -201,7 +209,9 @@ moe_status_t moe_grouped_swiglu(const moe_config_t *cfg, const void *x_perm,
  * Weighted combine [EP-add: the weighted expert output of each token;
  * EP-disp: combined with the routing weights]:
  *   out[t][:] = sum_{j=0}^{k-1} topk_w[t][j] * y_perm[pos[t*k+j]][:]
- * summed in slot order in fp32, then rounded to the act dtype.
+ * summed in slot order in fp32, then rounded to the act dtype.  With
+ * cfg->scale_inputs the weights were applied at dispatch: the rows are summed
+ * unweighted and topk_w is not read (may be NULL).
  * y_perm [P][d], pos [P] int32, topk_w [T][k] fp32, out [T][d] (written).
  */
 moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm,

@@ -86,7 +86,7 @@ def check_layer(moe, oracle, w, device="cuda", sample=None, max_experts=48, bias
     if bias is None and inp["bias"] is not None:
         bias = inp["bias"]
     bias_d = None if bias is None else bias.cuda()
-    layer = moe.MoELayer(Wr, Wgu, Wd, w.k, bias_d, w.renorm)
+    layer = moe.MoELayer(Wr, Wgu, Wd, w.k, bias_d, w.renorm, w.scale_inputs)
     out = layer(x)
     torch.cuda.synchronize()
     assert moe.moe_last_device_error() == moe.MOE_OK
@@ -133,7 +133,7 @@ def check_layer(moe, oracle, w, device="cuda", sample=None, max_experts=48, bias
     sel = torch.from_numpy(experts).long().cuda()
     Wgu_c, Wd_c = f32(Wgu[sel]), f32(Wd[sel])
     ref = oracle.token_outputs(np.arange(len(keep)), xs[keep], Wgu_c, Wd_c,
-                               remap[idx_ref[keep]], w_ref[keep])
+                               remap[idx_ref[keep]], w_ref[keep], scale_inputs=w.scale_inputs)
     got = f32(out[torch.from_numpy(tokens[keep]).cuda()]).astype(np.float64)
     err = np.abs(got - ref).max()
     assert np.isfinite(got).all()

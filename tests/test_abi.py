@@ -104,7 +104,8 @@ def test_workspace_too_small(moe):
     st = moe.moe_forward(cfg, 16, 16, None, 16, 16, 16, 16, need - 1, stream=0,
                          raise_on_error=False)
     assert st == moe.MOE_ERR_WORKSPACE
-    st = moe.moe_dispatch(cfg, 16, 16, 16, 16, 16, 16, 16, 16, 3, stream=0, raise_on_error=False)
+    st = moe.moe_dispatch(cfg, 16, None, 16, 16, 16, 16, 16, 16, 16, 3, stream=0,
+                          raise_on_error=False)
     assert st == moe.MOE_ERR_WORKSPACE
 
 
@@ -112,7 +113,7 @@ def test_empty_batch_is_a_no_op(moe):
     cfg = moe.config(0, 64, 8, 2, 64)
     assert moe.moe_forward(cfg, 16, 16, None, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
     assert moe.moe_route(cfg, 16, 16, None, 16, 16, 16, None, 0, stream=0) == moe.MOE_OK
-    assert moe.moe_dispatch(cfg, 16, 16, 16, 16, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
+    assert moe.moe_dispatch(cfg, 16, None, 16, 16, 16, 16, 16, 16, 16, 0, stream=0) == moe.MOE_OK
     assert moe.moe_grouped_swiglu(cfg, 16, 16, 16, 16, 16, 16, stream=0) == moe.MOE_OK
     assert moe.moe_combine(cfg, 16, 16, 16, 16, stream=0) == moe.MOE_OK
 
@@ -123,3 +124,12 @@ def test_raises_with_detail(moe):
         moe.moe_combine(cfg, None, 16, 16, 16, stream=0)
     assert ei.value.status == moe.MOE_ERR_INVALID_ARG
     assert "NULL" in str(ei.value)
+
+
+def test_input_scaling_needs_weights_at_dispatch_only(moe):
+    cfg = moe.config(16, 64, 8, 2, 64, scale_inputs=True)
+    ws = 1 << 20
+    st = moe.moe_dispatch(cfg, 16, None, 16, 16, 16, 16, 16, 16, 16, ws, stream=0,
+                          raise_on_error=False)
+    assert st == moe.MOE_ERR_INVALID_ARG  # scale_inputs without topk_w
+    assert "NULL" in moe.moe_last_error_message()

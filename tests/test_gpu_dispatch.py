@@ -35,7 +35,7 @@ def _run_dispatch(moe, idx, x, E):
     src = torch.full((P,), -1, dtype=torch.int32, device=dev)
     x_perm = torch.zeros(P, d, dtype=x.dtype, device=dev)
     ws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device=dev)
-    moe.moe_dispatch(cfg, torch.from_numpy(idx).cuda(), x.cuda(), counts, offsets, pos, src,
+    moe.moe_dispatch(cfg, torch.from_numpy(idx).cuda(), None, x.cuda(), counts, offsets, pos, src,
                      x_perm, ws)
     torch.cuda.synchronize()
     return counts.cpu().numpy(), offsets.cpu().numpy(), pos.cpu().numpy(), src.cpu().numpy(), \
@@ -82,3 +82,32 @@ def test_dispatch_flags_out_of_range_expert(moe, oracle):
     assert counts.sum() == T * k - 1 and offsets[-1] == T * k - 1
     assert pos[7 * k + 1] == -1
     assert moe.moe_last_device_error(raise_on_error=False) == moe.MOE_OK  # cleared
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_dispatch_scales_rows_when_weights_act_on_inputs(moe, oracle, dtype):
+    """scale_inputs: row r of x_perm is w[q] * x[t] formed in fp32 and rounded
+    once to the activation dtype (q the pair of row r, t its token)."""
+    T, E, k, d = 1500, 16, 4, 136
+    L = synth.make_logits(T, E, 41).numpy()
+    idx, w = oracle.topk(L, k, True)
+    x = torch.randn(T, d, generator=torch.Generator().manual_seed(3)).to(dtype)
+    wt = torch.from_numpy(w.astype(np.float32))
+    cfg = moe.config(T, d, E, k, 8, dtype, True, scale_inputs=True)
+    P = T * k
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pos = torch.empty(P, dtype=torch.int32, device="cuda")
+    src = torch.empty(P, dtype=torch.int32, device="cuda")
+    x_perm = torch.zeros(P, d, dtype=dtype, device="cuda")
+    ws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device="cuda")
+    moe.moe_dispatch(cfg, torch.from_numpy(idx).cuda(), wt.cuda(), x.cuda(), counts, offsets, pos,
+                     src, x_perm, ws)
+    torch.cuda.synchronize()
+    rc, ro, rp, rs = oracle.dispatch(idx, E)
+    np.testing.assert_array_equal(pos.cpu().numpy(), rp)
+    pair_of_row = np.empty(P, np.int64)
+    pair_of_row[rp] = np.arange(P)
+    expect = (x.float()[torch.from_numpy(rs).long()] *
+              wt.reshape(-1)[torch.from_numpy(pair_of_row)][:, None]).to(dtype)
+    assert torch.equal(x_perm.cpu(), expect)

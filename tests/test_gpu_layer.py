@@ -41,3 +41,20 @@ def test_layer_full_size_sampled(moe, oracle, name, sample):
     w = synth.WORKLOADS[name]
     n = check_layer(moe, oracle, w, sample=sample, max_experts=40)
     assert n >= 3
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_layer_weights_on_inputs(moe, oracle, dtype):
+    """Routing weights scale the expert inputs (experts receive tokens already
+    scaled by the router score); the combine sums unweighted."""
+    w = synth.WORKLOADS["tiny_fp32"].with_(dtype=dtype, scale_inputs=True, T=200)
+    assert check_layer(moe, oracle, w, device="cpu") >= 180
+
+
+def test_layer_no_dispatch_dense_form(moe, oracle):
+    """k = E with the weights on the inputs: every expert receives every token
+    scaled by its score -- the form with nothing to dispatch -- on a
+    Mixtral-shaped layer with a reduced hidden size."""
+    w = synth.Workload("dense_mixtral", 256, 512, 8, 8, 1792, "bf16", 44, renorm=False,
+                       scale_inputs=True)
+    check_layer(moe, oracle, w, device="cpu")

@@ -25,7 +25,7 @@ def lib():
     moe = load_moe()
     lib = ctypes.CDLL(moe.LIB_PATH)
     vp = ctypes.c_void_p
-    lib.moe_dispatch_noalloc.argtypes = [ctypes.POINTER(moe.moe_config_t)] + [vp] * 8
+    lib.moe_dispatch_noalloc.argtypes = [ctypes.POINTER(moe.moe_config_t)] + [vp] * 9
     lib.moe_dispatch_noalloc.restype = ctypes.c_int
     return moe, lib
 
@@ -41,7 +41,7 @@ def _outputs(T, E, k, d, dtype):
 
 def _noalloc(lib, cfg, idx, x, outs):
     moe, so = lib
-    p = [ctypes.c_void_p(t.data_ptr()) for t in [idx, x] + outs]
+    p = [ctypes.c_void_p(idx.data_ptr()), None] + [ctypes.c_void_p(t.data_ptr()) for t in [x] + outs]
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return so.moe_dispatch_noalloc(ctypes.byref(cfg), *p, stream)
 
@@ -60,7 +60,7 @@ def test_noalloc_matches_dispatch_twice(lib, oracle, T, E, k, d):
         ref = _outputs(T, E, k, d, dtype)
         ws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8,
                          device="cuda")
-        moe.moe_dispatch(cfg, idx, x, *ref, ws)
+        moe.moe_dispatch(cfg, idx, None, x, *ref, ws)
         got = _outputs(T, E, k, d, dtype)
         assert _noalloc(lib, cfg, idx, x, got) == moe.MOE_OK
         torch.cuda.synchronize()
@@ -87,4 +87,4 @@ def test_noalloc_empty_batch(lib):
     moe, so = lib
     cfg = moe.config(0, 8, 8, 2, 8, torch.bfloat16)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    assert so.moe_dispatch_noalloc(ctypes.byref(cfg), *([None] * 7), stream) == moe.MOE_OK
+    assert so.moe_dispatch_noalloc(ctypes.byref(cfg), *([None] * 8), stream) == moe.MOE_OK

@@ -27,7 +27,7 @@ combine_kernel(const TA *__restrict__ y_perm, const int32_t *__restrict__ pos,
     if (t >= T) return;  // warp-uniform
     if (lane < k) {
         s_pos[wid][lane] = pos[t * k + lane];
-        s_w[wid][lane] = w[t * k + lane];
+        s_w[wid][lane] = w ? w[t * k + lane] : 1.f;  // no weights: plain sum
     }
     __syncwarp();
     const int nvec = d / EPV;

@@ -170,6 +170,31 @@ gather_rows_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ po
     for (; i < row_vecs; i += 32) stg16(dst + i, ldg16(src + i));
 }
 
+// Scaled row gather x_perm[pos[q]] = scale[q] * x[q / k], the product formed
+// in fp32 and rounded once to the activation dtype.
+template <typename TA>
+__global__ void __launch_bounds__(kThreads)
+gather_rows_scaled_kernel(const TA *__restrict__ x, const int32_t *__restrict__ pos,
+                          const float *__restrict__ scale, int64_t P, int k, int d,
+                          TA *__restrict__ x_perm) {
+    constexpr int EPV = 16 / sizeof(TA);
+    const int lane = threadIdx.x & 31;
+    const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (q >= P) return;
+    const int row = pos[q];
+    if (row < 0) return;
+    const float wq = scale[q];
+    const TA *src = x + (q / k) * d;
+    TA *dst = x_perm + (int64_t)row * d;
+    for (int v = lane; v < d / EPV; v += 32) {
+        float f[EPV];
+        unpack16(ldg16(src + (int64_t)v * EPV), f, static_cast<const TA *>(nullptr));
+#pragma unroll
+        for (int i = 0; i < EPV; ++i) f[i] *= wq;
+        stg16(dst + (int64_t)v * EPV, pack16(f, static_cast<const TA *>(nullptr)));
+    }
+}
+
 }  // namespace
 
 DispatchGrid dispatch_grid(int64_t P) {
@@ -193,7 +218,8 @@ size_t dispatch_scratch_bytes(const Shape &s) {
 
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
-                            int32_t *hist, const DevStatus &ds, cudaStream_t st) {
+                            int32_t *hist, const DevStatus &ds, cudaStream_t st,
+                            const float *scale) {
     const int64_t P = s.P();
     const DispatchGrid g = dispatch_grid(P);
     chunk_histogram_kernel<<<g.blocks, kThreads, sizeof(int) * s.E, st>>>(idx, P, s.E, g.chunk,
@@ -209,8 +235,17 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
     if (!x_perm) return cudaSuccess;
     const int row_vecs = (int)((int64_t)s.d * (s.bf16 ? 2 : 4) / 16);
     const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
-    gather_rows_kernel<<<blocks, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), pos, P, s.k,
-                                                   row_vecs, static_cast<uint8_t *>(x_perm));
+    if (scale && s.bf16)
+        gather_rows_scaled_kernel<__nv_bfloat16><<<blocks, kThreads, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(x), pos, scale, P, s.k, s.d,
+            static_cast<__nv_bfloat16 *>(x_perm));
+    else if (scale)
+        gather_rows_scaled_kernel<float><<<blocks, kThreads, 0, st>>>(
+            static_cast<const float *>(x), pos, scale, P, s.k, s.d, static_cast<float *>(x_perm));
+    else
+        gather_rows_kernel<<<blocks, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), pos, P,
+                                                       s.k, row_vecs,
+                                                       static_cast<uint8_t *>(x_perm));
     return cudaGetLastError();
 }
 

@@ -35,9 +35,9 @@ std::mutex g_scratch_mutex;
 }  // namespace
 
 extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int32_t *topk_idx,
-                                             const void *x, int32_t *counts, int32_t *offsets,
-                                             int32_t *pos, int32_t *src_token, void *x_perm,
-                                             void *stream) {
+                                             const float *topk_w, const void *x, int32_t *counts,
+                                             int32_t *offsets, int32_t *pos, int32_t *src_token,
+                                             void *x_perm, void *stream) {
     const size_t need = moe_dispatch_workspace_size(cfg);
     if (need > kNoAllocScratchBytes) {
         moe::set_error_message(
@@ -70,6 +70,6 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int3
         }
         scratch = g_scratch_addr[dev];
     }
-    return moe_dispatch(cfg, topk_idx, x, counts, offsets, pos, src_token, x_perm,
+    return moe_dispatch(cfg, topk_idx, topk_w, x, counts, offsets, pos, src_token, x_perm,
                         scratch ? scratch : x_perm, kNoAllocScratchBytes, stream);
 }

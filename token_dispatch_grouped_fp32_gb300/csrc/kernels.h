@@ -13,6 +13,7 @@ struct Shape {
     int d, E, k, f;
     bool bf16;    // activation dtype: bf16 (else fp32)
     bool renorm;  // renormalise the chosen k weights
+    bool scale_inputs;  // routing weights scale expert inputs (dispatch), not outputs
     int64_t P() const { return T * (int64_t)k; }
 };
 
@@ -53,9 +54,11 @@ struct DispatchGrid {
 DispatchGrid dispatch_grid(int64_t P);
 size_t dispatch_scratch_bytes(const Shape &s);  // per-block histogram ints
 // x_perm == nullptr: counts, offsets, pos and src_token only (no row gather).
+// scale != nullptr: each gathered row is multiplied by its pair's weight.
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
-                            int32_t *hist, const DevStatus &ds, cudaStream_t st);
+                            int32_t *hist, const DevStatus &ds, cudaStream_t st,
+                            const float *scale = nullptr);
 
 // Grouped SwiGLU experts.  bf16: tcgen05 tensor-core path; fp32: SIMT path.
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
@@ -65,7 +68,8 @@ cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const
                                       const float *Wgu, const float *Wd, float *h_perm,
                                       float *y_perm, cudaStream_t st);
 
-// Weighted combine of the expert rows back into token order.
+// Weighted combine of the expert rows back into token order (w == nullptr:
+// unweighted sum).
 cudaError_t launch_combine(const Shape &s, const void *y_perm, const int32_t *pos, const float *w,
                            void *out, cudaStream_t st);
 

@@ -114,6 +114,7 @@ moe_status_t check_cfg(const moe_config_t *cfg, Shape *s) {
     s->f = cfg->f;
     s->bf16 = cfg->act_dtype == MOE_BF16;
     s->renorm = cfg->renormalize != 0;
+    s->scale_inputs = cfg->scale_inputs != 0;
     return MOE_OK;
 }
 
@@ -298,9 +299,10 @@ moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits,
                      "top-k launch");
 }
 
-moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, const void *x,
-                          int32_t *counts, int32_t *offsets, int32_t *pos, int32_t *src_token,
-                          void *x_perm, void *ws, size_t ws_bytes, void *stream) {
+moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, const float *topk_w,
+                          const void *x, int32_t *counts, int32_t *offsets, int32_t *pos,
+                          int32_t *src_token, void *x_perm, void *ws, size_t ws_bytes,
+                          void *stream) {
     g_msg[0] = 0;
     Shape s;
     moe_status_t st = check_cfg(cfg, &s);
@@ -308,6 +310,7 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, cons
     if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
     if ((st = check_ptrs({topk_idx, x, counts, offsets, pos, src_token, x_perm, ws})) != MOE_OK)
         return st;
+    if (s.scale_inputs && (st = check_ptrs({topk_w})) != MOE_OK) return st;
     if (ws_bytes < dispatch_scratch_bytes(s)) {
         set_error_message("workspace %zu bytes < %zu needed", ws_bytes, dispatch_scratch_bytes(s));
         return MOE_ERR_WORKSPACE;
@@ -316,7 +319,8 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx, cons
     if ((st = device_status(&ds)) != MOE_OK) return st;
     return from_cuda(launch_dispatch(s, topk_idx, x, counts, offsets, pos, src_token, x_perm,
                                      static_cast<int32_t *>(ws), ds,
-                                     static_cast<cudaStream_t>(stream)),
+                                     static_cast<cudaStream_t>(stream),
+                                     s.scale_inputs ? topk_w : nullptr),
                      "dispatch launch");
 }
 
@@ -343,10 +347,12 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm, const int3
     moe_status_t st = check_cfg(cfg, &s);
     if (st != MOE_OK) return st;
     if (s.T == 0) return MOE_OK;  // empty batch: nothing to check or launch
-    if ((st = check_ptrs({y_perm, pos, topk_w, out})) != MOE_OK) return st;
+    if ((st = check_ptrs({y_perm, pos, out})) != MOE_OK) return st;
+    if (!s.scale_inputs && (st = check_ptrs({topk_w})) != MOE_OK) return st;
     DevStatus ds;
     if ((st = device_status(&ds)) != MOE_OK) return st;
-    return from_cuda(launch_combine(s, y_perm, pos, topk_w, out, static_cast<cudaStream_t>(stream)),
+    return from_cuda(launch_combine(s, y_perm, pos, s.scale_inputs ? nullptr : topk_w, out,
+                                    static_cast<cudaStream_t>(stream)),
                      "combine launch");
 }
 
@@ -383,12 +389,14 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
         MOE_OK)
         return st;
     if ((st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm,
-                                        at<int32_t>(ws, L.hist), ds, cs),
+                                        at<int32_t>(ws, L.hist), ds, cs,
+                                        s.scale_inputs ? w : nullptr),
                         "dispatch launch")) != MOE_OK)
         return st;
     if ((st = run_experts(s, x_perm, offsets, W_gate_up, W_down, h_perm, y_perm, ds, cs)) != MOE_OK)
         return st;
-    return from_cuda(launch_combine(s, y_perm, pos, w, out, cs), "combine launch");
+    return from_cuda(launch_combine(s, y_perm, pos, s.scale_inputs ? nullptr : w, out, cs),
+                     "combine launch");
 }
 
 moe_status_t moe_forward_host(const moe_config_t *cfg, const void *x_host, const float *Wr,

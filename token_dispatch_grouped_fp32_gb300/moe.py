@@ -39,7 +39,7 @@ class MoEError(RuntimeError):
 class moe_config_t(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("k", ctypes.c_int32), ("f", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
-                ("renormalize", ctypes.c_int32)]
+                ("renormalize", ctypes.c_int32), ("scale_inputs", ctypes.c_int32)]
 
 
 def _load():
@@ -58,7 +58,7 @@ def _load():
         "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "moe_route_workspace_size": ([cfgp], sz),
         "moe_route_from_logits": ([cfgp, vp, vp, vp, vp], st),
-        "moe_dispatch": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
+        "moe_dispatch": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "moe_grouped_swiglu": ([cfgp, vp, vp, vp, vp, vp, vp, vp], st),
         "moe_combine": ([cfgp, vp, vp, vp, vp, vp], st),
         "moe_forward": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
@@ -108,14 +108,15 @@ def _check(status: int, where: str, raise_on_error: bool):
 
 
 def config(T: int, d: int, E: int, k: int, f: int, dtype=torch.bfloat16,
-           renormalize: bool = True) -> moe_config_t:
+           renormalize: bool = True, scale_inputs: bool = False) -> moe_config_t:
     if dtype in (torch.bfloat16, "bf16", MOE_BF16):
         act = MOE_BF16
     elif dtype in (torch.float32, "f32", MOE_F32):
         act = MOE_F32
     else:
         act = int(dtype)
-    return moe_config_t(int(T), int(d), int(E), int(k), int(f), act, int(bool(renormalize)))
+    return moe_config_t(int(T), int(d), int(E), int(k), int(f), act, int(bool(renormalize)),
+                        int(bool(scale_inputs)))
 
 
 def moe_status_string(status: int) -> str:
@@ -161,13 +162,13 @@ def moe_route_from_logits(cfg, logits, topk_idx, topk_w, stream=None, raise_on_e
     return _check(s, "moe_route_from_logits", raise_on_error)
 
 
-def moe_dispatch(cfg, topk_idx, x, counts, offsets, pos, src_token, x_perm, ws, ws_bytes=None,
-                 stream=None, raise_on_error=True):
+def moe_dispatch(cfg, topk_idx, topk_w, x, counts, offsets, pos, src_token, x_perm, ws,
+                 ws_bytes=None, stream=None, raise_on_error=True):
     if ws_bytes is None:
         ws_bytes = 0 if ws is None or isinstance(ws, int) else ws.numel() * ws.element_size()
-    s = _lib.moe_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts), _ptr(offsets),
-                          _ptr(pos), _ptr(src_token), _ptr(x_perm), _ptr(ws), int(ws_bytes),
-                          _stream(stream))
+    s = _lib.moe_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(topk_w), _ptr(x), _ptr(counts),
+                          _ptr(offsets), _ptr(pos), _ptr(src_token), _ptr(x_perm), _ptr(ws),
+                          int(ws_bytes), _stream(stream))
     return _check(s, "moe_dispatch", raise_on_error)
 
 
@@ -214,7 +215,8 @@ class MoELayer:
     W_gate_up [E, d, 2f] and W_down [E, f, d] in the activation dtype,
     optional per-expert logit bias [E] fp32."""
 
-    def __init__(self, Wr, W_gate_up, W_down, k, logit_bias=None, renormalize=True):
+    def __init__(self, Wr, W_gate_up, W_down, k, logit_bias=None, renormalize=True,
+                 scale_inputs=False):
         self.Wr, self.W_gate_up, self.W_down = Wr, W_gate_up, W_down
         self.logit_bias = logit_bias
         self.E, self.d = Wr.shape
@@ -222,10 +224,12 @@ class MoELayer:
         self.k = int(k)
         self.dtype = W_gate_up.dtype
         self.renormalize = renormalize
+        self.scale_inputs = scale_inputs
         self._ws = None
 
     def config(self, T: int) -> moe_config_t:
-        return config(T, self.d, self.E, self.k, self.f, self.dtype, self.renormalize)
+        return config(T, self.d, self.E, self.k, self.f, self.dtype, self.renormalize,
+                      self.scale_inputs)
 
     def workspace(self, T: int):
         need = moe_workspace_size(self.config(T))

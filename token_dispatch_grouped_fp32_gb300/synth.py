@@ -45,6 +45,7 @@ class Workload:
     seed: int
     renorm: bool = True
     zipf: bool = False
+    scale_inputs: bool = False  # routing weights on the expert inputs
     down_std_from_f: bool = False
 
     def with_tokens(self, T: int) -> "Workload":
