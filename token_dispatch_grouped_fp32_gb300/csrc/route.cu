@@ -327,6 +327,27 @@ cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const 
 
 constexpr int kNoExpert = 0x7fffffff;
 
+// The rank order as one unsigned 64-bit key: an order-preserving image of
+// the float in the high word (+0.0 and -0.0 alike, a NaN lowest) and the
+// complement of the expert id in the low word (so the lower id wins ties).
+// key(a, ia) > key(b, ib) exactly when ranks_before(a, ia, b, ib); 0 means
+// "no candidate".
+__device__ __forceinline__ unsigned long long select_key(float v, int e) {
+    uint32_t o = 0u;
+    if (!isnan(v)) {
+        const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+        o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    }
+    return ((unsigned long long)o << 32) | (0xFFFFFFFFu - (uint32_t)e);
+}
+__device__ __forceinline__ float key_value(unsigned long long key) {
+    const uint32_t o = (uint32_t)(key >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+__device__ __forceinline__ int key_expert(unsigned long long key) {
+    return (int)(0xFFFFFFFFu - (uint32_t)key);
+}
+
 // With nparts > 0 the logits are first formed as the sum of nparts partial
 // buffers (stride T*E, added in buffer order) plus bias, and written to
 // `logits`; the selection then uses exactly the written values.
@@ -372,32 +393,25 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
     for (int i = 0; i < VPL; ++i)
         if (!((avail >> i) & 1u)) v[i] = -INFINITY;
 
+    unsigned long long key[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) key[i] = select_key(v[i], lane + 32 * i);
     float my_v = 0.f;
     int my_e = 0;
     for (int j = 0; j < k; ++j) {
-        float bv = NAN;
-        int be = kNoExpert;
+        unsigned long long best = 0ull;
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            if (!((avail >> i) & 1u)) continue;
-            int e = lane + 32 * i;
-            if (be == kNoExpert || ranks_before(v[i], e, bv, be)) {
-                bv = v[i];
-                be = e;
-            }
-        }
+        for (int i = 0; i < VPL; ++i)
+            if ((avail >> i) & 1u) best = key[i] > best ? key[i] : best;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (oe != kNoExpert && (be == kNoExpert || ranks_before(ov, oe, bv, be))) {
-                bv = ov;
-                be = oe;
-            }
+            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
         }
-        if (be != kNoExpert && (be & 31) == lane) avail &= ~(1u << (be >> 5));
+        const int be = key_expert(best);
+        if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
         if (lane == j) {
-            my_v = bv;
+            my_v = key_value(best);
             my_e = be;
         }
     }
