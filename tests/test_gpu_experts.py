@@ -29,6 +29,11 @@ EXPERT_CASES = [
     ([0, 700, 1030, 5, 1500], 264, 200),
     ([600, 0, 900], 128, 384),
     ([2049], 64, 136),
+    # K above 3072: the per-row epilogue store (shorter K uses transposed stores)
+    ([3, 130, 0, 70], 3136, 136),       # gate/up K = 3136, down K = 136
+    ([1, 90, 40], 96, 3136),            # down K = 3136
+    ([520, 0, 530], 3136, 72),          # CTA pairs, gate/up K = 3136
+    ([520, 530], 64, 3200),             # CTA pairs, down K = 3200
 ]
 
 

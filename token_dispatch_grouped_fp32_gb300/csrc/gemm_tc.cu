@@ -99,9 +99,51 @@ struct Params {
     int n_out;    // output columns (f for G1, d for G2)
     int f;        // column offset of the up half in Wgu (G1)
     int n_tiles;  // column tiles per row tile
+    int transpose_epi;  // epilogue store pattern (see kTransposeMaxK)
     __nv_bfloat16 *out;  // [P][n_out]
     DevStatus ds;
 };
+
+// Epilogue store pattern (Params::transpose_epi): 0 = each thread stores its
+// own row (16-byte stores, 32 rows per warp instruction); 1 = 32 x 32 blocks
+// of packed bf16 pairs are transposed with shuffles so each warp instruction
+// stores 128 contiguous bytes of one row.  The second costs shuffles but
+// fewer memory transactions; it pays when epilogues are frequent relative to
+// the main loop (short K).
+constexpr int kTransposeMaxK = 3072;
+
+// 32 x 32 transpose across the warp: before, lane l holds v[i] = M[l][i];
+// after, lane l holds v[i] = M[i][l].
+__device__ __forceinline__ void transpose32(uint32_t (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            if (i & s) continue;
+            const uint32_t send = upper ? v[i] : v[i + s];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, s);
+            if (upper) v[i] = recv;
+            else v[i + s] = recv;
+        }
+    }
+}
+
+// Lane l holds packed[i] = bf16 pair (columns 2i, 2i+1 of a 64-column block)
+// of row (rbase + l).  Transpose so lane l holds pair l of rows rbase..+31 and
+// store each row's 128 bytes with one warp instruction.
+__device__ __forceinline__ void store_rows_transposed(uint32_t (&packed)[32], __nv_bfloat16 *out,
+                                                      int64_t rbase, int rows_valid, int col0,
+                                                      int n_out) {
+    transpose32(packed);
+    const int lane = threadIdx.x & 31;
+    const int col = col0 + 2 * lane;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (i < rows_valid && col + 2 <= n_out)
+            *reinterpret_cast<uint32_t *>(out + (rbase + i) * n_out + col) = packed[i];
+}
 
 struct TileInfo {
     int e, row0, rows, n_blk;  // row0/rows: the tile's slice of expert e's segment
@@ -347,7 +389,49 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint32_t t_row = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
             const bool row_ok = r_in_tile < ti.rows;
             __nv_bfloat16 *orow = p.out + (int64_t)(ti.row0 + r_in_tile) * p.n_out;
-            if (SWIGLU) {
+            if (p.transpose_epi) {
+                // rows of this warp: ti.row0 + rank*BM + quarter*32 + (0..31)
+                const int wrow0 = (int)rank * BM + quarter * 32;
+                const int rows_valid = max(0, min(32, ti.rows - wrow0));
+                const int64_t rbase = (int64_t)ti.row0 + wrow0;
+                const int ncols = SWIGLU ? BN / 2 : BN;
+                const int n0 = ti.n_blk * ncols;
+#pragma unroll 1
+                for (int c = 0; c < ncols; c += 64) {
+                    uint32_t packed[32];
+                    if (SWIGLU) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t g[32], u[32];
+                            tmem_ld32(t_row + c + 32 * half, g);
+                            tmem_ld32(t_row + BN / 2 + c + 32 * half, u);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+                                float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                                __nv_bfloat162 b2 = __floats2bfloat162_rn(g0 / (1.f + __expf(-g0)) * u0,
+                                                                          g1 / (1.f + __expf(-g1)) * u1);
+                                packed[16 * half + i] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            uint32_t y[32];
+                            tmem_ld32(t_row + c + 32 * half, y);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(y[2 * i]),
+                                                                          __uint_as_float(y[2 * i + 1]));
+                                packed[16 * half + i] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                        }
+                    }
+                    store_rows_transposed(packed, p.out, rbase, rows_valid, n0 + c, p.n_out);
+                }
+            } else if (SWIGLU) {
                 const int n0 = ti.n_blk * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
@@ -478,6 +562,7 @@ cudaError_t run(const Shape &s, int units, const CUtensorMap &mx, const CUtensor
     p1.n_out = s.f;
     p1.f = s.f;
     p1.n_tiles = (int)n_tiles1;
+    p1.transpose_epi = s.d <= kTransposeMaxK;
     p1.out = static_cast<__nv_bfloat16 *>(h_perm);
     p1.ds = ds;
     const unsigned g1 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles1);
@@ -488,6 +573,7 @@ cudaError_t run(const Shape &s, int units, const CUtensorMap &mx, const CUtensor
     p2.n_out = s.d;
     p2.f = 0;
     p2.n_tiles = (int)n_tiles2;
+    p2.transpose_epi = s.f <= kTransposeMaxK;
     p2.out = static_cast<__nv_bfloat16 *>(y_perm);
     const unsigned g2 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles2);
     return launch<false, CTAS>(g2, mh, mwd, p2, st);
