@@ -37,10 +37,11 @@
 // is persistent (as many CTAs or pairs as fit at once) and strides over the
 // tile list.
 //
-// Roles (192 threads per CTA): warp 0 issues TMA loads, warp 1 owns the
-// tensor memory and issues the MMAs and their commits (in a pair: the leader
-// only, commits multicast to both CTAs, and every load of both CTAs signals
-// the leader's full barrier), warps 2-5 run the epilogue (tensor memory ->
+// Roles (192 threads per CTA): one thread of warp 0 issues the TMA loads,
+// warp 1 owns the tensor memory and one of its threads issues the MMAs and
+// their commits (in a pair: the leader only, commits multicast to both CTAs,
+// and every load of both CTAs signals the leader's full barrier), warps 2-5
+// run the epilogue (tensor memory ->
 // registers -> global), each on its 32-lane quarter of its CTA's
 // accumulator.  Two accumulators (2 x 256 columns) let the epilogue of one
 // tile overlap the main loop of the next.
@@ -246,36 +247,37 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const int total = s_tile[E] * n_tiles;
     const int nk = (p.K + BK - 1) / BK;
 
+    // The producer and the MMA issuer are single threads (lane 0 of warps 0
+    // and 1): a warp-wide loop (a shuffle of each wait's result and a
+    // reconvergence per K step) left the tensor pipe idle ~8 % of the time,
+    // because the issuing thread keeps at most about one MMA queued ahead.
     if (warp == 0) {
         // ------------------------- TMA producer -------------------------
-        int s = 0;
-        uint32_t ph = 0;
-        uint32_t issued = 0, last_par = 0;  // per stage armed here: ever / parity of last phase
-        bool ok = true;
-        for (int tile = unit; tile < total && ok; tile += nunits) {
-            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles, C::TILE_M);
-            // first B column of this CTA: in G1 the gate columns come first and the
-            // up columns (offset f) follow; a pair splits them between its CTAs
-            int n0;
-            if (SWIGLU) n0 = ti.n_blk * (BN / 2) + (PAIR && !leader ? p.f : 0);
-            else n0 = ti.n_blk * BN + (int)rank * (BN / 2);
-            const int arow = ti.row0 + (int)rank * BM;
-            for (int ks = 0; ks < nk; ++ks) {
-                int good = 1;
-                if (lane == 0) good = wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort);
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = sig_full + 8 * s;
-                const int k0 = ks * BK;
-                if (lane == 0 && leader) {
-                    mbar_arrive_expect_tx(bar_full + 8 * s, C::EXPECT_BYTES);
-                    issued |= 1u << s;
-                    last_par = (last_par & ~(1u << s)) | (ph << s);
-                }
-                if (lane == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0, last_par = 0;  // per stage armed here: ever / parity of last phase
+            bool ok = true;
+            for (int tile = unit; tile < total && ok; tile += nunits) {
+                const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles, C::TILE_M);
+                // first B column of this CTA: in G1 the gate columns come first and the
+                // up columns (offset f) follow; a pair splits them between its CTAs
+                int n0;
+                if (SWIGLU) n0 = ti.n_blk * (BN / 2) + (PAIR && !leader ? p.f : 0);
+                else n0 = ti.n_blk * BN + (int)rank * (BN / 2);
+                const int arow = ti.row0 + (int)rank * BM;
+                for (int ks = 0; ks < nk; ++ks) {
+                    if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = sig_full + 8 * s;
+                    const int k0 = ks * BK;
+                    if (leader) {
+                        mbar_arrive_expect_tx(bar_full + 8 * s, C::EXPECT_BYTES);
+                        issued |= 1u << s;
+                        last_par = (last_par & ~(1u << s)) | (ph << s);
+                    }
                     tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, &tmA, k0, arow, fb);
                     const uint32_t bdst = base_s + C::OFF_B + s * C::B_BYTES;
 #pragma unroll
@@ -284,28 +286,27 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         if (SWIGLU && !PAIR && a >= 2) col = ti.n_blk * (BN / 2) + p.f + 64 * (a - 2);
                         tma_load_3d<CTAS>(bdst + a * B_ATOM_BYTES, &tmB, col, k0, ti.e, fb);
                     }
-                }
-                __syncwarp();
-                if (++s == STAGES) {
-                    s = 0;
-                    ph ^= 1u;
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
-        }
-        // drain: every phase armed here must have received all of its bytes
-        if (leader && lane == 0) {
-            for (int i = 0; i < STAGES; ++i)
-                if ((issued >> i) & 1u) {
-                    volatile int never = 0;
-                    if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never,
-                                      drain_limit(p.ds)))
-                        break;
-                }
+            // drain: every phase armed here must have received all of its bytes
+            if (leader) {
+                for (int i = 0; i < STAGES; ++i)
+                    if ((issued >> i) & 1u) {
+                        volatile int never = 0;
+                        if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never,
+                                          drain_limit(p.ds)))
+                            break;
+                    }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------- MMA issuer ---------------------------
-        if (leader) {
+        if (leader && lane == 0) {
             int s = 0;
             uint32_t ph = 0;
             int it = 0;
@@ -323,56 +324,42 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                 // test hook: wait on the drain barrier, which nothing signals
                 // before the issuer's own final commit, so the wait runs out
                 // and the kernel takes its abort path before any MMA
-                int good = 1;
-                if (lane == 0) good = wait_bounded(bar_drain, 0, p.ds, s_abort);
-                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                ok = wait_bounded(bar_drain, 0, p.ds, s_abort);
             }
             for (int tile = unit; tile < total && ok; tile += nunits, ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-                int good = 1;
-                if (lane == 0) good = wait_bounded(bar_tempty + 8 * acc, aph ^ 1u, p.ds, s_abort);
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) break;
+                if (!wait_bounded(bar_tempty + 8 * acc, aph ^ 1u, p.ds, s_abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int ks = 0; ks < nk; ++ks) {
-                    good = 1;
-                    if (lane == 0) good = wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort);
-                    good = __shfl_sync(0xffffffffu, good, 0);
-                    if (!good) {
+                    if (!wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t a_st = adesc0 + (uint64_t)((s * A_BYTES) >> 4);
-                        const uint64_t b_st = bdesc0 + (uint64_t)((s * C::B_BYTES) >> 4);
+                    const uint64_t a_st = adesc0 + (uint64_t)((s * A_BYTES) >> 4);
+                    const uint64_t b_st = bdesc0 + (uint64_t)((s * C::B_BYTES) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                            mma_bf16<CTAS>(d_tmem, a_st + (uint64_t)((kk * 32) >> 4),
-                                           b_st + (uint64_t)((kk * 2048) >> 4), C::IDESC,
-                                           (ks | kk) != 0 ? 1u : 0u);
-                        mma_commit_all<CTAS>(bar_empty + 8 * s);  // frees the stage (both CTAs)
-                    }
-                    __syncwarp();
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                        mma_bf16<CTAS>(d_tmem, a_st + (uint64_t)((kk * 32) >> 4),
+                                       b_st + (uint64_t)((kk * 2048) >> 4), C::IDESC,
+                                       (ks | kk) != 0 ? 1u : 0u);
+                    mma_commit_all<CTAS>(bar_empty + 8 * s);  // frees the stage (both CTAs)
                     if (++s == STAGES) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
                 if (!ok) break;
-                if (lane == 0) mma_commit_all<CTAS>(bar_tfull + 8 * acc);  // accumulators ready
-                __syncwarp();
+                mma_commit_all<CTAS>(bar_tfull + 8 * acc);  // accumulators ready
             }
             // drain: every MMA issued here completes before tensor memory is freed
-            if (lane == 0) {
-                mma_commit_local<CTAS>(bar_drain);
-                volatile int never = 0;
-                wait_bounded(bar_drain, 0, p.ds, &never, drain_limit(p.ds));
-            }
-            __syncwarp();
+            mma_commit_local<CTAS>(bar_drain);
+            volatile int never = 0;
+            wait_bounded(bar_drain, 0, p.ds, &never, drain_limit(p.ds));
         }
+        __syncwarp();
     } else {
         // --------------------------- epilogue ----------------------------
         const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
