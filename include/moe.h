@@ -124,8 +124,9 @@ size_t moe_route_workspace_size(const moe_config_t *cfg);
  * ws         at least moe_route_workspace_size(cfg) bytes, 256-byte aligned
  *            (may be NULL when that size is 0)
  * The selection is made on exactly the fp32 values written to `logits`.
- * For bf16 x with 64 <= E <= 256 (E % 16 == 0, d % 64 == 0) the products are
- * formed on the tensor cores: Wr is split into three bf16 terms
+ * For bf16 x, d % 64 == 0 and either 64 <= E <= 256 or (8 <= E < 64 and
+ * T >= 1024), with E % 8 == 0, the products are formed on the tensor cores:
+ * Wr is split into three bf16 terms
  * (w = w1 + w2 + w3, ~2^-25 relative), each product with the exact bf16 x is
  * exact, and accumulation is fp32; otherwise fp32 FMAs on the CUDA cores.
  */

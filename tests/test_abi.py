@@ -44,7 +44,10 @@ def test_workspace_sizes(moe):
     ws = moe.moe_workspace_size(cfg)
     P = 4096 * 2
     perm = 2 * P * (4096 + 14336 + 4096)
-    assert perm <= ws <= perm + 4096 * 8 * 4 + 10 * P * 4 + 64 * 1024
+    # + logits, routing and dispatch arrays, and the tensor-core router's scratch:
+    # the three-term split weight (E x 3d bf16) and its K-split partial logits
+    router = 3 * 8 * 4096 * 2 + 32 * 4096 * 8 * 4
+    assert perm <= ws <= perm + 4096 * 8 * 4 + 10 * P * 4 + router + 64 * 1024
     assert moe.moe_workspace_size(moe.config(0, 4096, 8, 2, 14336)) == 0
     assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * ((P + 2047) // 2048)
     # invalid config -> 0
@@ -84,9 +87,13 @@ def test_null_and_misaligned_pointers(moe):
 
 
 def test_route_workspace_size(moe):
-    # CUDA-core logits (E <= 32, or fp32 activations) need no workspace
-    assert moe.moe_route_workspace_size(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 0
+    # CUDA-core logits (fp32 activations, or E <= 32 with a small batch) need no workspace
+    assert moe.moe_route_workspace_size(moe.config(512, 4096, 8, 2, 14336, "bf16")) == 0
     assert moe.moe_route_workspace_size(moe.config(64, 128, 128, 2, 256, "f32")) == 0
+    assert moe.moe_route_workspace_size(moe.config(4096, 4096, 33, 2, 14336, "bf16")) == 0
+    # E = 8 at T = 4096 runs on the tensor cores (N padded to 16)
+    n8 = moe.moe_route_workspace_size(moe.config(4096, 4096, 8, 2, 14336, "bf16"))
+    assert 8 * 3 * 4096 * 2 + 4096 * 8 * 4 <= n8 <= 8 * 3 * 4096 * 2 + 256 + 64 * 4096 * 8 * 4
     # tensor-core logits: split weight (E*3d bf16) + fp32 partial logits
     T, d, E = 8192, 7168, 256
     n = moe.moe_route_workspace_size(moe.config(T, d, E, 8, 2048, "bf16"))

@@ -1,8 +1,8 @@
 """Router parity: top-k indices bit-exact and weights within the fp32 bound
 against the oracle on the same fp32 logit buffer; router logits within the
-fp32 summation bound, on both logit paths (CUDA-core FMAs for E <= 32 or
-fp32 x; tensor cores with the three-term bf16 split of Wr for bf16 x and
-64 <= E <= 256)."""
+fp32 summation bound, on both logit paths (CUDA-core FMAs for fp32 x and
+small batches with E <= 32; tensor cores with the three-term bf16 split of
+Wr for bf16 x, 8 <= E <= 256, E % 8 == 0)."""
 import numpy as np
 import pytest
 import torch
@@ -53,7 +53,7 @@ def test_route_from_logits_matches_oracle(moe, oracle, T, E, k, ties, renorm):
 
 @pytest.mark.parametrize("name,T", [("tiny_fp32", 64), ("mixtral", 512), ("gptoss_prefill", 700),
                                     ("qwen3_zipf", 1500), ("deepseek", 300), ("gptoss_decode", 64),
-                                    ("deepseek", 8192)])
+                                    ("deepseek", 8192), ("mixtral", 4096), ("mixtral", 1500)])
 def test_route_logits_and_selection(moe, oracle, name, T):
     w = synth.WORKLOADS[name].with_tokens(T)
     inp = synth.make_inputs(w, weights=False)
@@ -88,3 +88,38 @@ def test_route_logits_and_selection(moe, oracle, name, T):
         assert near_tie(ref_L[t], w.k, tol[t]) or \
             sorted(g_idx[t].tolist()) == sorted(ref_idx[t].tolist()), t
     assert len(differ) <= max(2, T // 200)
+
+
+# Tensor-core logit shapes: N = E rounded up to 16, three W' tiles per stage
+# for N <= 128 (x read once), one per stage above; row tiles ragged at T.
+TC_SHAPES = [
+    # T, d, E, k
+    (1024, 256, 8, 2),
+    (1100, 512, 24, 3),
+    (2000, 128, 40, 4),
+    (1500, 320, 48, 6),
+    (1024, 64, 64, 8),
+    (1030, 192, 136, 4),
+    (1024, 64, 256, 8),
+]
+
+
+@pytest.mark.parametrize("T,d,E,k", TC_SHAPES)
+def test_route_tensor_core_shapes(moe, oracle, T, d, E, k):
+    w = synth.Workload("tc_shape", T, d, E, k, 8, "bf16", 31 + E)
+    inp = synth.make_inputs(w, weights=False)
+    x, Wr = inp["x"], inp["Wr"]
+    cfg = moe.config(T, d, E, k, 8, torch.bfloat16, True)
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(256, moe.moe_route_workspace_size(cfg)), dtype=torch.uint8, device="cuda")
+    moe.moe_route(cfg, x.cuda(), Wr.cuda(), None, logits, idx, wt, ws)
+    torch.cuda.synchronize()
+    xs, Wrs = f32(x), f32(Wr)
+    ref_L = oracle.router_logits(xs, Wrs, None)
+    tol = logit_tolerance(xs, Wrs, None)
+    assert (np.abs(logits.cpu().numpy().astype(np.float64) - ref_L) <= tol).all()
+    ref_idx, ref_w = oracle.topk(logits.cpu().numpy(), k, True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.abs(wt.cpu().numpy().astype(np.float64) - ref_w).max() <= weight_tolerance(E)

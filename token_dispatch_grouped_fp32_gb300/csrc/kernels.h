@@ -35,8 +35,8 @@ cudaError_t launch_topk_partials(const Shape &s, const float *partial, int split
 
 // Router logits on the tensor cores (bf16 x, fp32 Wr split into 3 bf16 terms).
 struct RouterTcPlan {
-    int ks_total;      // K steps of 64 over K' = 3d
-    int ks_per_split;  // K steps per CTA
+    int ks_total;      // pipeline stages of a row tile: d / 64 (three W' tiles each) or 3d / 64
+    int ks_per_split;  // stages per CTA
     int splits;        // K splits (blockIdx.y)
 };
 bool router_tc_eligible(const Shape &s);

@@ -1,5 +1,5 @@
 // router_tc.cu -- router logits on the sm_103a tensor cores, for bf16
-// activations and 64 <= E <= 256 experts.
+// activations and 8 <= E <= 256 experts (E a multiple of 8).
 //
 // Transformers docs "Expert parallelism", section "Adding an implementation":
 // the router produces the logits from which top_k_index and top_k_weights are
@@ -13,14 +13,17 @@
 //     L = x . w1 + x . w2 + x . w3
 // is an fp32-accumulated dot product of x with w, like the SIMT kernel's,
 // at a fraction of its cost.  The three terms are laid side by side along K
-// (W' = [w1 | w2 | w3], E x 3d), so the router is one GEMM with K' = 3d whose
-// A tile at k' is x's tile at k' mod d.
+// (W' = [w1 | w2 | w3], E x 3d).
 //
 // Layout: A = x (K-major, TMA box 64 x 128 tokens), B = W' (K-major, box
-// 64 x E), M = 128 tokens, N = E, K step 64, four pipeline stages.  K' is
-// split over blockIdx.y so the grid fills the GPU; each split writes fp32
-// partial logits [split][T][E], which the top-k kernel adds in split order
-// (a fixed order, so results are reproducible) before selecting.
+// 64 x N with N = E rounded up to 16; rows past E read zeros), M = 128
+// tokens.  For N <= 128 a pipeline stage holds one x tile and the three
+// W' tiles of the same 64 columns of d, so x is read once and each stage
+// issues 12 MMAs; for larger N a stage holds one x tile and one W' tile
+// (K' = 3d in steps of 64, x read three times).  K is split over
+// blockIdx.y so the grid fills the GPU; each split writes fp32 partial
+// logits [split][T][E], which the top-k kernel adds in split order (a fixed
+// order, so results are reproducible) before selecting.
 #include <cuda.h>
 
 #include <algorithm>
@@ -35,18 +38,36 @@ namespace {
 using namespace tc;
 
 constexpr int RBM = 128;   // tokens per tile (MMA M)
-constexpr int RBK = 64;    // K elements per stage (128 bytes of bf16)
-constexpr int RSTAGES = 4;
+constexpr int RBK = 64;    // K elements per W' / x tile (128 bytes of bf16)
+constexpr int R_MAX_STAGES = 6;
 constexpr int R_A_BYTES = RBM * RBK * 2;        // 16 KB
-constexpr int R_B_MAX_BYTES = 256 * RBK * 2;    // 32 KB for E = 256
 constexpr int R_THREADS = 128;
-constexpr int R_OFF_A = 0;
-constexpr int R_OFF_B = RSTAGES * R_A_BYTES;
-constexpr int R_OFF_BAR = R_OFF_B + RSTAGES * R_B_MAX_BYTES;
-constexpr int R_NUM_BARS = 2 * RSTAGES + 2;  // full, empty, done, drain
-constexpr int R_OFF_TMEM = R_OFF_BAR + R_NUM_BARS * 8;
-constexpr int R_OFF_ABORT = R_OFF_TMEM + 4;
-constexpr int R_SMEM_BYTES = R_OFF_ABORT + 4 + 1024;
+constexpr int R_NUM_BARS = 2 * R_MAX_STAGES + 2;  // full, empty, done, drain
+constexpr int R_SMEM_MAX = 200 * 1024;
+
+// Shared-memory plan of one launch (host and device agree on it).
+struct RouterSmem {
+    int n_pad;        // MMA N: E rounded up to 16
+    int terms;        // W' tiles per stage: 3 (N <= 128) or 1
+    int stages;
+    int stage_bytes;  // one x tile + `terms` W' tiles
+    int off_bar, off_tmem, off_abort, bytes;
+};
+
+inline RouterSmem router_smem(int E) {
+    RouterSmem m;
+    m.n_pad = (E + 15) / 16 * 16;
+    m.terms = m.n_pad <= 128 ? 3 : 1;
+    m.stage_bytes = R_A_BYTES + m.terms * m.n_pad * RBK * 2;
+    // small stages: keep two CTAs per SM; large ones: one CTA with 3-4 stages
+    const int budget = m.stage_bytes <= 32 * 1024 ? 96 * 1024 : 192 * 1024;
+    m.stages = std::max(2, std::min(R_MAX_STAGES, budget / m.stage_bytes));
+    m.off_bar = m.stages * m.stage_bytes;
+    m.off_tmem = m.off_bar + R_NUM_BARS * 8;
+    m.off_abort = m.off_tmem + 4;
+    m.bytes = m.off_abort + 4 + 1024;  // + alignment slack
+    return m;
+}
 
 // W'[e][j*d + i] = j-th bf16 term of Wr[e][i], j = 0, 1, 2.
 __global__ void split_router_weight_kernel(const float *__restrict__ Wr, int64_t n, int d,
@@ -71,7 +92,8 @@ struct RouterParams {
     float *partial;   // [splits][T][E]
     int64_t T;
     int d, E;
-    int ks_per_split, ks_total;
+    int ks_per_split, ks_total;  // stages of this tile's K loop, per split / in all
+    int n_pad, terms, stages, stage_bytes, off_bar, off_tmem, off_abort;
     uint32_t idesc;
     uint32_t tmem_cols;
     DevStatus ds;
@@ -84,23 +106,24 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_s - raw_s);
-    const uint32_t bar_full = base_s + R_OFF_BAR;
-    const uint32_t bar_empty = bar_full + 8 * RSTAGES;
-    const uint32_t bar_done = bar_empty + 8 * RSTAGES;
+    const int S = p.stages;
+    const uint32_t bar_full = base_s + p.off_bar;
+    const uint32_t bar_empty = bar_full + 8 * S;
+    const uint32_t bar_done = bar_empty + 8 * S;
     const uint32_t bar_drain = bar_done + 8;
-    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + R_OFF_TMEM);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(base + R_OFF_ABORT);
+    volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + p.off_tmem);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(base + p.off_abort);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m0 = (int64_t)blockIdx.x * RBM;
     const int split = blockIdx.y;
     const int ks0 = split * p.ks_per_split;
     const int ks1 = min(ks0 + p.ks_per_split, p.ks_total);
-    const uint32_t b_bytes = (uint32_t)p.E * RBK * 2;
+    const uint32_t w_tile_bytes = (uint32_t)p.n_pad * RBK * 2;
 
     if (threadIdx.x == 0) {
         *s_abort = 0;
-        for (int i = 0; i < RSTAGES; ++i) {
+        for (int i = 0; i < S; ++i) {
             mbar_init(bar_full + 8 * i, 1);
             mbar_init(bar_empty + 8 * i, 1);
         }
@@ -109,7 +132,7 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 0) tmem_alloc<1>(base_s + R_OFF_TMEM, p.tmem_cols);
+    if (warp == 0) tmem_alloc<1>(base_s + p.off_tmem, p.tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -124,18 +147,27 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
             for (int ks = ks0; ks < ks1; ++ks) {
                 if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort)) break;
                 const uint32_t fb = bar_full + 8 * s;
-                mbar_arrive_expect_tx(fb, R_A_BYTES + b_bytes);
-                const int kp = ks * RBK;  // column of W' (K' = 3d)
-                tma_load_2d<1>(base_s + R_OFF_A + s * R_A_BYTES, &tmX, kp % p.d, (int)m0, fb);
-                tma_load_2d<1>(base_s + R_OFF_B + s * R_B_MAX_BYTES, &tmW, kp, 0, fb);
+                const uint32_t st = base_s + (uint32_t)(s * p.stage_bytes);
+                mbar_arrive_expect_tx(fb, R_A_BYTES + p.terms * w_tile_bytes);
+                if (p.terms == 3) {
+                    // x columns [64 ks, 64 ks + 64) and the three W' tiles that meet them
+                    const int kx = ks * RBK;
+                    tma_load_2d<1>(st, &tmX, kx, (int)m0, fb);
+                    for (int j = 0; j < 3; ++j)
+                        tma_load_2d<1>(st + R_A_BYTES + j * w_tile_bytes, &tmW, j * p.d + kx, 0, fb);
+                } else {
+                    const int kp = ks * RBK;  // column of W' (K' = 3d)
+                    tma_load_2d<1>(st, &tmX, kp % p.d, (int)m0, fb);
+                    tma_load_2d<1>(st + R_A_BYTES, &tmW, kp, 0, fb);
+                }
                 issued |= 1u << s;
                 last_par = (last_par & ~(1u << s)) | (ph << s);
-                if (++s == RSTAGES) {
+                if (++s == S) {
                     s = 0;
                     ph ^= 1u;
                 }
             }
-            for (int i = 0; i < RSTAGES; ++i)  // drain: every armed copy lands
+            for (int i = 0; i < S; ++i)  // drain: every armed copy lands
                 if ((issued >> i) & 1u) {
                     volatile int never = 0;
                     if (!wait_bounded(bar_full + 8 * i, (last_par >> i) & 1u, p.ds, &never,
@@ -149,8 +181,8 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         if (lane == 0) {
             // A and B are both K-major: 128-byte rows, 8-row groups 1024 B
             // apart; a K step of 16 elements is 32 bytes along the row.
-            const uint64_t adesc0 = smem_desc_sw128(base_s + R_OFF_A, 16, 1024);
-            const uint64_t bdesc0 = smem_desc_sw128(base_s + R_OFF_B, 16, 1024);
+            const uint64_t adesc0 = smem_desc_sw128(base_s, 16, 1024);
+            const uint64_t bdesc0 = smem_desc_sw128(base_s + R_A_BYTES, 16, 1024);
             int s = 0;
             uint32_t ph = 0;
             for (int ks = ks0; ks < ks1; ++ks) {
@@ -159,15 +191,16 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     break;
                 }
                 tc_fence_after();
-                const uint64_t a_st = adesc0 + (uint64_t)((s * R_A_BYTES) >> 4);
-                const uint64_t b_st = bdesc0 + (uint64_t)((s * R_B_MAX_BYTES) >> 4);
+                const uint64_t a_st = adesc0 + (uint64_t)((s * p.stage_bytes) >> 4);
+                const uint64_t b_st = bdesc0 + (uint64_t)((s * p.stage_bytes) >> 4);
+                for (int j = 0; j < p.terms; ++j)
 #pragma unroll
-                for (int kk = 0; kk < RBK / 16; ++kk)
-                    mma_bf16<1>(tmem, a_st + (uint64_t)((kk * 32) >> 4),
-                                b_st + (uint64_t)((kk * 32) >> 4), p.idesc,
-                                (ks > ks0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < RBK / 16; ++kk)
+                        mma_bf16<1>(tmem, a_st + (uint64_t)((kk * 32) >> 4),
+                                    b_st + (uint64_t)((j * w_tile_bytes + kk * 32) >> 4), p.idesc,
+                                    (ks > ks0 || j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_all<1>(bar_empty + 8 * s);
-                if (++s == RSTAGES) {
+                if (++s == S) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -189,13 +222,14 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
         for (int c = 0; c < p.E; c += 32) {
             uint32_t v[32];
-            tmem_ld32(taddr + c, v);
+            tmem_ld32(taddr + c, v);  // columns past N are allocated, never stored
             tmem_ld_wait();
             if (t < p.T) {
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
-                    *reinterpret_cast<uint4 *>(row + c + 4 * q) =
-                        make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                    if (c + 4 * q < p.E)  // E is a multiple of 8
+                        *reinterpret_cast<uint4 *>(row + c + 4 * q) =
+                            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
             }
         }
     }
@@ -208,16 +242,22 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
 }  // namespace
 
 bool router_tc_eligible(const Shape &s) {
-    return s.bf16 && s.E >= 64 && s.E <= 256 && s.E % 16 == 0 && s.d % RBK == 0;
+    if (!s.bf16 || s.E < 8 || s.E > 256 || s.E % 8 != 0 || s.d % RBK != 0) return false;
+    // up to 32 experts the CUDA-core kernel also selects in the same launch,
+    // which wins for small batches
+    return s.E >= 64 || s.T >= 1024;
 }
 
 RouterTcPlan router_tc_plan(const Shape &s) {
     RouterTcPlan pl;
+    const RouterSmem m = router_smem(s.E);
     const int64_t tiles = (s.T + RBM - 1) / RBM;
-    pl.ks_total = 3 * s.d / RBK;
-    // enough CTAs for two per SM-wave of 152 SMs, at least 4 K steps each
+    pl.ks_total = (m.terms == 3 ? 1 : 3) * s.d / RBK;
+    // enough CTAs for two per SM-wave of 152 SMs, with at least 2 stages
+    // (three W' tiles each) or 4 stages (one W' tile each) per CTA
+    const int min_stages = m.terms == 3 ? 2 : 4;
     int64_t want = (304 + tiles - 1) / tiles;
-    want = std::max<int64_t>(1, std::min<int64_t>(want, std::max(1, pl.ks_total / 4)));
+    want = std::max<int64_t>(1, std::min<int64_t>(want, std::max(1, pl.ks_total / min_stages)));
     pl.ks_per_split = (int)((pl.ks_total + want - 1) / want);
     pl.splits = (pl.ks_total + pl.ks_per_split - 1) / pl.ks_per_split;
     return pl;
@@ -241,7 +281,7 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
     if (!attr_set[dev]) {
         if ((err = cudaFuncSetAttribute(router_logits_tc_kernel,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        R_SMEM_BYTES)) != cudaSuccess)
+                                        R_SMEM_MAX)) != cudaSuccess)
             return err;
         attr_set[dev] = true;
     }
@@ -258,9 +298,10 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
         Wr, n, s.d, wsplit);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
+    const RouterSmem m = router_smem(s.E);
     CUtensorMap mx, mw;
     if (!tensor_map_rows(&mx, x, s.T, s.d, RBM) ||
-        !tensor_map_rows(&mw, wsplit, s.E, 3 * (int64_t)s.d, (uint32_t)s.E)) {
+        !tensor_map_rows(&mw, wsplit, s.E, 3 * (int64_t)s.d, (uint32_t)m.n_pad)) {
         set_error_message("cuTensorMapEncodeTiled rejected a router operand");
         return cudaErrorInvalidValue;
     }
@@ -271,11 +312,18 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
     p.E = s.E;
     p.ks_per_split = pl.ks_per_split;
     p.ks_total = pl.ks_total;
-    p.idesc = idesc_bf16(RBM, s.E, false);
-    p.tmem_cols = s.E <= 32 ? 32 : s.E <= 64 ? 64 : s.E <= 128 ? 128 : 256;
+    p.n_pad = m.n_pad;
+    p.terms = m.terms;
+    p.stages = m.stages;
+    p.stage_bytes = m.stage_bytes;
+    p.off_bar = m.off_bar;
+    p.off_tmem = m.off_tmem;
+    p.off_abort = m.off_abort;
+    p.idesc = idesc_bf16(RBM, m.n_pad, false);
+    p.tmem_cols = m.n_pad <= 32 ? 32 : m.n_pad <= 64 ? 64 : m.n_pad <= 128 ? 128 : 256;
     p.ds = ds;
     dim3 grid((unsigned)((s.T + RBM - 1) / RBM), (unsigned)pl.splits);
-    router_logits_tc_kernel<<<grid, R_THREADS, R_SMEM_BYTES, st>>>(mx, mw, p);
+    router_logits_tc_kernel<<<grid, R_THREADS, m.bytes, st>>>(mx, mw, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     *partial_out = partial;
     *splits_out = pl.splits;
