@@ -49,7 +49,10 @@ def test_workspace_sizes(moe):
     router = 3 * 8 * 4096 * 2 + 32 * 4096 * 8 * 4
     assert perm <= ws <= perm + 4096 * 8 * 4 + 10 * P * 4 + router + 64 * 1024
     assert moe.moe_workspace_size(moe.config(0, 4096, 8, 2, 14336)) == 0
-    assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * ((P + 2047) // 2048)
+    # P = 8192 pairs in chunks of 256 (the smallest chunk that keeps <= 256 chunks)
+    assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * (P // 256)
+    big = moe.config(70000, 8, 1024, 8, 8)  # 560,000 pairs: chunks of 2048
+    assert moe.moe_dispatch_workspace_size(big) == 4 * 1024 * ((560000 + 2047) // 2048)
     # invalid config -> 0
     assert moe.moe_workspace_size(moe.config(4, 4096, 8, 9, 14336)) == 0
 

@@ -197,9 +197,14 @@ gather_rows_scaled_kernel(const TA *__restrict__ x, const int32_t *__restrict__ 
 
 }  // namespace
 
-DispatchGrid dispatch_grid(int64_t P) {
+DispatchGrid dispatch_grid(int64_t P, int E) {
+    // Chunks of 2048 pairs; 256 when the E x chunks histogram stays small
+    // (few experts and pairs): the histogram and scatter blocks are latency
+    // bound, so more and shorter blocks finish sooner, while the single-block
+    // scan over E x chunks entries must stay short (at E = 128-256 and 64K+
+    // pairs, 256-pair chunks made the scan the slowest step).
     DispatchGrid g;
-    g.chunk = 2048;
+    g.chunk = (int64_t)E * ((P + 255) / 256) <= 4096 ? 256 : 2048;
     int64_t nb = (P + g.chunk - 1) / g.chunk;
     if (nb > 1024) {
         int64_t c = (P + 1023) / 1024;
@@ -212,7 +217,7 @@ DispatchGrid dispatch_grid(int64_t P) {
 }
 
 size_t dispatch_scratch_bytes(const Shape &s) {
-    DispatchGrid g = dispatch_grid(s.P());
+    DispatchGrid g = dispatch_grid(s.P(), s.E);
     return sizeof(int32_t) * (size_t)s.E * (size_t)g.blocks;
 }
 
@@ -221,7 +226,7 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
                             const float *scale) {
     const int64_t P = s.P();
-    const DispatchGrid g = dispatch_grid(P);
+    const DispatchGrid g = dispatch_grid(P, s.E);
     chunk_histogram_kernel<<<g.blocks, kThreads, sizeof(int) * s.E, st>>>(idx, P, s.E, g.chunk,
                                                                         g.blocks, hist, ds);
     cudaError_t err = cudaGetLastError();

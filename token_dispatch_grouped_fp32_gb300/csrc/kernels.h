@@ -51,7 +51,7 @@ struct DispatchGrid {
     int chunk;  // pairs per block (multiple of 256)
     int blocks;  // number of blocks (>= 1 when P > 0)
 };
-DispatchGrid dispatch_grid(int64_t P);
+DispatchGrid dispatch_grid(int64_t P, int E);
 size_t dispatch_scratch_bytes(const Shape &s);  // per-block histogram ints
 // x_perm == nullptr: counts, offsets, pos and src_token only (no row gather).
 // scale != nullptr: each gathered row is multiplied by its pair's weight.
