@@ -194,12 +194,17 @@ def run_reference(args, w):
     del inp["Wgu"], inp["Wd"]
     bias = None if inp["bias"] is None else inp["bias"].float().cpu().numpy()
     oracle.build()
-    # size each step to ~ args.ref_step_s seconds of host work
+    # size each step to ~ step_s seconds of host work, so that the whole run
+    # (K steps) stays near two minutes: 4 s per step for a few steps, down to
+    # 0.25 s per step for long runs
+    step_s = args.ref_step_s
+    if step_s is None:
+        step_s = min(4.0, max(0.25, 120.0 / max(1, args.steps)))
     n = min(w.T, 4)
     t0 = time.perf_counter()
     oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
     dt = time.perf_counter() - t0
-    n = int(max(1, min(w.T, n * args.ref_step_s / max(dt, 1e-6))))
+    n = int(max(1, min(w.T, n * step_s / max(dt, 1e-6))))
     for _ in range(args.warmup if args.ref_warmup else 0):
         oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
     times = []
@@ -474,7 +479,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None, help="override T")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-step-s", type=float, default=4.0)
+    ap.add_argument("--ref-step-s", type=float, default=None,
+                    help="host seconds per reference step (default: 120 s / steps, within 0.25-4 s)")
     ap.add_argument("--ref-warmup", action="store_true",
                     help="run the warm-up steps in the reference arm too")
     args = ap.parse_args(argv)
