@@ -69,22 +69,23 @@ inline RouterSmem router_smem(int E) {
     return m;
 }
 
-// W'[e][j*d + i] = j-th bf16 term of Wr[e][i], j = 0, 1, 2.
-__global__ void split_router_weight_kernel(const float *__restrict__ Wr, int64_t n, int d,
+// W'[e][j*d + i] = j-th bf16 term of Wr[e][i], j = 0, 1, 2.  Grid: x over
+// the d columns, y over the experts (no integer division per element).
+__global__ void split_router_weight_kernel(const float *__restrict__ Wr, int d,
                                            __nv_bfloat16 *__restrict__ Wsplit) {
-    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n;
-         q += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t e = q / d, i = q - e * d;
-        const float w = Wr[q];
+    const int e = blockIdx.y;
+    const float *src = Wr + (int64_t)e * d;
+    __nv_bfloat16 *row = Wsplit + (int64_t)e * 3 * d;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x) {
+        const float w = src[i];
         const __nv_bfloat16 w1 = __float2bfloat16_rn(w);
         const float r1 = w - __bfloat162float(w1);
         const __nv_bfloat16 w2 = __float2bfloat16_rn(r1);
         const float r2 = r1 - __bfloat162float(w2);
         const __nv_bfloat16 w3 = __float2bfloat16_rn(r2);
-        __nv_bfloat16 *row = Wsplit + e * 3 * (int64_t)d;
         row[i] = w1;
         row[d + i] = w2;
-        row[2 * (int64_t)d + i] = w3;
+        row[2 * d + i] = w3;
     }
 }
 
@@ -293,9 +294,8 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
     __nv_bfloat16 *wsplit = static_cast<__nv_bfloat16 *>(scratch);
     float *partial = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
                                                (((size_t)s.E * 3 * s.d * 2 + 255) & ~(size_t)255));
-    const int64_t n = (int64_t)s.E * s.d;
-    split_router_weight_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(
-        Wr, n, s.d, wsplit);
+    split_router_weight_kernel<<<dim3((unsigned)std::min(8, (s.d + 255) / 256), (unsigned)s.E), 256, 0,
+                                 st>>>(Wr, s.d, wsplit);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     const RouterSmem m = router_smem(s.E);
