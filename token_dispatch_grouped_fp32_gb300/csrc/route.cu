@@ -371,7 +371,10 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
         if (e < E) avail |= 1u << i;
     }
     if (nparts > 0) {
-        // remaining partial buffers, each added to all VPL values at once
+        // remaining partial buffers, each added to all VPL values at once, in
+        // buffer order; unrolled so that the loads of several buffers are in
+        // flight together (the adds stay in order)
+#pragma unroll 4
         for (int q = 1; q < nparts; ++q) {
             const float *pq = partial + (int64_t)q * T * E + t * E;
 #pragma unroll
