@@ -34,9 +34,9 @@ EXPERT_CASES = [
     ([1, 90, 40], 96, 3136),            # down K = 3136
     ([520, 0, 530], 3136, 72),          # CTA pairs, gate/up K = 3136
     ([520, 530], 64, 3200),             # CTA pairs, down K = 3200
-    # CTA pairs: last row tiles of <= 128 rows run as M = 128 half tiles
-    ([1100, 620, 1200, 0], 200, 328),   # tails 76 and 108 (half), 176 (full)
-    ([128, 129, 1, 1800], 72, 136),     # a 128-row expert (one half tile), 129 rows (full)
+    # CTA pairs whose experts end in short row tiles (76, 108, 176 rows; 128, 129, 1)
+    ([1100, 620, 1200, 0], 200, 328),
+    ([128, 129, 1, 1800], 72, 136),
 ]
 
 
