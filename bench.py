@@ -31,7 +31,6 @@ if ROOT not in sys.path:
 
 METRIC = "MoE-layer tokens/s on 1 GB300; GEMM % tensor peak, permute/combine % HBM BW"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 9  # logits, top-k, histogram, scan, scatter, gather, G1, G2, combine
 
 
 # --------------------------------------------------------------------------
@@ -442,7 +441,7 @@ def run_ours(args, w):
                     "mode": "moe_forward_host, steps alternating on two streams (copies of one "
                             "step overlap the other's layer)",
                     "serial_value": aggregate_throughput(T, world, e2e_serial / 1e3)},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": moe.moe_forward_kernel_launches(cfg) * args.steps,
             "clocks": clocks.summary(), "wall_s_timed_region": t_wall,
         }
         print(json.dumps(line), flush=True)

@@ -100,6 +100,14 @@ size_t moe_workspace_size(const moe_config_t *cfg);
 size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
 
 /*
+ * Number of kernel launches one moe_forward call makes for `cfg`: the router
+ * (1 to 3 launches, by path), the dispatch (4), the two grouped GEMMs (2) and
+ * the combine (1).  0 when T == 0; -1 for an invalid configuration.  Makes
+ * no CUDA call.
+ */
+int moe_forward_kernel_launches(const moe_config_t *cfg);
+
+/*
  * Bytes of workspace moe_route needs for `cfg`: 0 when the logits are
  * computed on the CUDA cores (fp32 activations, E < 64 or E > 256, E not a
  * multiple of 16, or d not a multiple of 64); otherwise the three-term bf16

@@ -143,3 +143,16 @@ def test_input_scaling_needs_weights_at_dispatch_only(moe):
                           raise_on_error=False)
     assert st == moe.MOE_ERR_INVALID_ARG  # scale_inputs without topk_w
     assert "NULL" in moe.moe_last_error_message()
+
+
+def test_forward_kernel_launches(moe):
+    """The bench's gpu_launches claim comes from the library's own launch plan."""
+    # Mixtral-shaped, bf16, E = 8, T = 4096: tensor-core router (weight split,
+    # logits, top-k) + dispatch (4) + G1, G2 + combine
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 10
+    # small batch, E <= 32: logits and selection in one CUDA-core launch
+    assert moe.moe_forward_kernel_launches(moe.config(64, 128, 8, 2, 256, "f32")) == 8
+    # fp32 activations, E > 32: CUDA-core logits, then the top-k kernel
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 128, 64, 2, 256, "f32")) == 9
+    assert moe.moe_forward_kernel_launches(moe.config(0, 128, 8, 2, 256, "bf16")) == 0
+    assert moe.moe_forward_kernel_launches(moe.config(4, 4096, 8, 9, 14336)) == -1

@@ -250,6 +250,16 @@ size_t moe_dispatch_workspace_size(const moe_config_t *cfg) {
     return dispatch_scratch_bytes(s);
 }
 
+int moe_forward_kernel_launches(const moe_config_t *cfg) {
+    Shape s;
+    if (check_cfg(cfg, &s) != MOE_OK) return -1;
+    if (s.T == 0) return 0;
+    // the same choices as run_route: tensor cores (weight split, logits, top-k),
+    // CUDA cores selecting in the logits launch, or CUDA-core logits + top-k
+    const int route = router_tc_eligible(s) ? 3 : router_selects_in_logits(s) ? 1 : 2;
+    return route + 4 /* histogram, scan, scatter, gather */ + 2 /* G1, G2 */ + 1 /* combine */;
+}
+
 void moe_set_wait_limit_ns(uint64_t ns) {
     g_wait_limit_ns.store(ns ? ns : 2000000000ull, std::memory_order_relaxed);
 }

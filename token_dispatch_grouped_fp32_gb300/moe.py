@@ -55,6 +55,7 @@ def _load():
         "moe_last_error_message": ([], ctypes.c_char_p),
         "moe_workspace_size": ([cfgp], sz),
         "moe_dispatch_workspace_size": ([cfgp], sz),
+        "moe_forward_kernel_launches": ([cfgp], st),
         "moe_route": ([cfgp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "moe_route_workspace_size": ([cfgp], sz),
         "moe_route_from_logits": ([cfgp, vp, vp, vp, vp], st),
@@ -133,6 +134,10 @@ def moe_workspace_size(cfg: moe_config_t) -> int:
 
 def moe_dispatch_workspace_size(cfg: moe_config_t) -> int:
     return int(_lib.moe_dispatch_workspace_size(ctypes.byref(cfg)))
+
+
+def moe_forward_kernel_launches(cfg: moe_config_t) -> int:
+    return int(_lib.moe_forward_kernel_launches(ctypes.byref(cfg)))
 
 
 def moe_set_wait_limit_ns(ns: int) -> None:
