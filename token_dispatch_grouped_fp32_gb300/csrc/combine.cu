@@ -19,6 +19,7 @@ template <typename TA>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const TA *__restrict__ y_perm, const int32_t *__restrict__ pos,
                const float *__restrict__ w, int64_t T, int k, int d, TA *__restrict__ out) {
+    pdl_entry();
     constexpr int EPV = 16 / sizeof(TA);
     __shared__ int s_pos[kWarps][kMaxK];
     __shared__ float s_w[kWarps][kMaxK];
@@ -70,11 +71,11 @@ cudaError_t launch_combine(const Shape &s, const void *y_perm, const int32_t *po
                            void *out, cudaStream_t st) {
     const unsigned blocks = (unsigned)((s.T + kWarps - 1) / kWarps);
     if (s.bf16)
-        combine_kernel<__nv_bfloat16><<<blocks, kThreads, 0, st>>>(
+        launch_pdl(combine_kernel<__nv_bfloat16>, dim3(blocks), dim3(kThreads), 0, st,
             static_cast<const __nv_bfloat16 *>(y_perm), pos, w, s.T, s.k, s.d,
             static_cast<__nv_bfloat16 *>(out));
     else
-        combine_kernel<float><<<blocks, kThreads, 0, st>>>(static_cast<const float *>(y_perm), pos,
+        launch_pdl(combine_kernel<float>, dim3(blocks), dim3(kThreads), 0, st, static_cast<const float *>(y_perm), pos,
                                                           w, s.T, s.k, s.d,
                                                           static_cast<float *>(out));
     return cudaGetLastError();

@@ -81,4 +81,34 @@ __device__ __forceinline__ void stg16(void *p, const uint4 &v) {
     *reinterpret_cast<uint4 *>(p) = v;
 }
 
+// Programmatic dependent launch.  Every kernel of the layer starts with
+// pdl_entry(): it lets the next kernel in the stream be scheduled (once all
+// of this grid's blocks have started, so a dependent never takes SMs from
+// this grid's own blocks), then waits until the previous kernel in the
+// stream has completed and its writes are visible.  Nothing is read from
+// earlier kernels before that wait.  Launched without the attribute (or
+// after a copy), both instructions are no-ops.
+__device__ __forceinline__ void pdl_entry() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization (see pdl_entry); extra
+// attributes (a cluster shape) may be appended.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 }  // namespace moe

@@ -24,6 +24,7 @@ constexpr int kWarps = kThreads / 32;
 __global__ void __launch_bounds__(kThreads)
 chunk_histogram_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB,
                        int32_t *__restrict__ hist, DevStatus ds) {
+    pdl_entry();
     extern __shared__ int sh_count[];
     for (int e = threadIdx.x; e < E; e += kThreads) sh_count[e] = 0;
     __syncthreads();
@@ -46,6 +47,7 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kScanThreads)
 scan_kernel(int32_t *__restrict__ hist, int E, int NB, int32_t *__restrict__ counts,
             int32_t *__restrict__ offsets) {
+    pdl_entry();
     __shared__ int warp_tot[kScanThreads / 32];
     __shared__ int total_s;
     const int n = E * NB;
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(kThreads)
 scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chunk, int NB,
                const int32_t *__restrict__ base, int32_t *__restrict__ pos,
                int32_t *__restrict__ src_token) {
+    pdl_entry();
     extern __shared__ int sh_warp[];  // [kWarps][E]: per-warp counts, then running row
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kWarps * E; i += kThreads) sh_warp[i] = 0;
@@ -150,6 +153,7 @@ scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chu
 __global__ void __launch_bounds__(kThreads)
 gather_rows_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ pos, int64_t P,
                    int k, int row_vecs, uint8_t *__restrict__ x_perm) {
+    pdl_entry();
     const int lane = threadIdx.x & 31;
     const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (q >= P) return;
@@ -177,6 +181,7 @@ __global__ void __launch_bounds__(kThreads)
 gather_rows_scaled_kernel(const TA *__restrict__ x, const int32_t *__restrict__ pos,
                           const float *__restrict__ scale, int64_t P, int k, int d,
                           TA *__restrict__ x_perm) {
+    pdl_entry();
     constexpr int EPV = 16 / sizeof(TA);
     const int lane = threadIdx.x & 31;
     const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
@@ -227,28 +232,28 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
                             const float *scale) {
     const int64_t P = s.P();
     const DispatchGrid g = dispatch_grid(P, s.E);
-    chunk_histogram_kernel<<<g.blocks, kThreads, sizeof(int) * s.E, st>>>(idx, P, s.E, g.chunk,
+    launch_pdl(chunk_histogram_kernel, dim3(g.blocks), dim3(kThreads), sizeof(int) * s.E, st, idx, P, s.E, g.chunk,
                                                                         g.blocks, hist, ds);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    scan_kernel<<<1, kScanThreads, 0, st>>>(hist, s.E, g.blocks, counts, offsets);
+    launch_pdl(scan_kernel, dim3(1), dim3(kScanThreads), 0, st, hist, s.E, g.blocks, counts, offsets);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t sh = sizeof(int) * (size_t)kWarps * s.E;
-    scatter_kernel<<<g.blocks, kThreads, sh, st>>>(idx, P, s.k, s.E, g.chunk, g.blocks, hist, pos,
+    launch_pdl(scatter_kernel, dim3(g.blocks), dim3(kThreads), sh, st, idx, P, s.k, s.E, g.chunk, g.blocks, hist, pos,
                                                   src_token);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (!x_perm) return cudaSuccess;
     const int row_vecs = (int)((int64_t)s.d * (s.bf16 ? 2 : 4) / 16);
     const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
     if (scale && s.bf16)
-        gather_rows_scaled_kernel<__nv_bfloat16><<<blocks, kThreads, 0, st>>>(
+        launch_pdl(gather_rows_scaled_kernel<__nv_bfloat16>, dim3(blocks), dim3(kThreads), 0, st,
             static_cast<const __nv_bfloat16 *>(x), pos, scale, P, s.k, s.d,
             static_cast<__nv_bfloat16 *>(x_perm));
     else if (scale)
-        gather_rows_scaled_kernel<float><<<blocks, kThreads, 0, st>>>(
+        launch_pdl(gather_rows_scaled_kernel<float>, dim3(blocks), dim3(kThreads), 0, st,
             static_cast<const float *>(x), pos, scale, P, s.k, s.d, static_cast<float *>(x_perm));
     else
-        gather_rows_kernel<<<blocks, kThreads, 0, st>>>(static_cast<const uint8_t *>(x), pos, P,
+        launch_pdl(gather_rows_kernel, dim3(blocks), dim3(kThreads), 0, st, static_cast<const uint8_t *>(x), pos, P,
                                                        s.k, row_vecs,
                                                        static_cast<uint8_t *>(x_perm));
     return cudaGetLastError();

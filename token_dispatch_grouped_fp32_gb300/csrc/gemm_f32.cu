@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kThreads)
 grouped_gemm_f32_kernel(const float *__restrict__ A, const int32_t *__restrict__ offsets, int E,
                         const float *__restrict__ B, int K, int Nb, int N, int f,
                         float *__restrict__ C) {
+    pdl_entry();
     extern __shared__ int s_dyn[];
     int *s_off = s_dyn;
     int *s_tile = s_dyn + (E + 1);
@@ -147,12 +148,12 @@ cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const
     const int64_t mtiles = (P + BM - 1) / BM + s.E;  // upper bound of sum_e ceil(count_e / BM)
     const size_t sh = sizeof(int) * (2 * (size_t)s.E + 2);
     dim3 g1((unsigned)mtiles, (unsigned)((s.f + BN - 1) / BN));
-    grouped_gemm_f32_kernel<true><<<g1, kThreads, sh, st>>>(x_perm, offsets, s.E, Wgu, s.d,
+    launch_pdl(grouped_gemm_f32_kernel<true>, dim3(g1), dim3(kThreads), sh, st, x_perm, offsets, s.E, Wgu, s.d,
                                                            2 * s.f, s.f, s.f, h_perm);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     dim3 g2((unsigned)mtiles, (unsigned)((s.d + BN - 1) / BN));
-    grouped_gemm_f32_kernel<false><<<g2, kThreads, sh, st>>>(h_perm, offsets, s.E, Wd, s.f, s.d,
+    launch_pdl(grouped_gemm_f32_kernel<false>, dim3(g2), dim3(kThreads), sh, st, h_perm, offsets, s.E, Wd, s.f, s.d,
                                                             s.d, 0, y_perm);
     return cudaGetLastError();
 }

@@ -179,6 +179,7 @@ template <bool SWIGLU, int CTAS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, Params p) {
+    pdl_entry();
     using C = Cfg<CTAS>;
     constexpr bool PAIR = C::PAIR;
     constexpr int STAGES = C::STAGES;
@@ -511,15 +512,17 @@ cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttri
     attr[0].val.clusterDim.x = CTAS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_entry
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cfg;
 }
 
 template <bool SWIGLU, int CTAS>
 cudaError_t launch(unsigned grid, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p,
                    cudaStream_t st) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<CTAS>(grid, st, attr);
     return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, CTAS>, ta, tb, p);
 }
@@ -529,7 +532,7 @@ template <bool SWIGLU, int CTAS> cudaError_t prepare(int *resident_units) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            Cfg<CTAS>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<CTAS>(CTAS, nullptr, attr);
     return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<SWIGLU, CTAS>,
                                           &cfg);

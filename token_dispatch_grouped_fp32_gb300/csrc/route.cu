@@ -73,6 +73,7 @@ router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ W
                            const float *__restrict__ bias, float *__restrict__ logits,
                            int64_t T, int d, int E, int k, int renorm,
                            int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+    pdl_entry();
     constexpr int TPW = 32 / EP;
     __shared__ float red[kSplitWarps][32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -198,6 +199,7 @@ __global__ void __launch_bounds__(256)
 router_logits_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
                      const float *__restrict__ bias, float *__restrict__ logits, int64_t T, int d,
                      int E) {
+    pdl_entry();
     static_assert((BM / TM) * (BN / TN) == 256, "256 threads");
     constexpr int BK = kLogitBK;
     constexpr int RG = BM / TM;  // row groups
@@ -284,7 +286,7 @@ template <typename TA, int BM, int BN, int TM, int TN>
 cudaError_t launch_logits_cfg(const Shape &s, const TA *x, const float *Wr, const float *bias,
                               float *logits, cudaStream_t st) {
     dim3 grid((unsigned)((s.T + BM - 1) / BM), (unsigned)((s.E + BN - 1) / BN));
-    router_logits_kernel<TA, BM, BN, TM, TN><<<grid, 256, 0, st>>>(x, Wr, bias, logits, s.T, s.d, s.E);
+    launch_pdl(router_logits_kernel<TA, BM, BN, TM, TN>, dim3(grid), dim3(256), 0, st, x, Wr, bias, logits, s.T, s.d, s.E);
     return cudaGetLastError();
 }
 
@@ -296,7 +298,7 @@ cudaError_t launch_logits_split(const Shape &s, const TA *x, const float *Wr, co
     // with a single expert group (E <= 32) the kernel also selects; larger E
     // leaves the selection to the top-k kernel
     const bool fused = grid.y == 1 && idx != nullptr;
-    router_logits_split_kernel<TA, EP><<<grid, 256, 0, st>>>(
+    launch_pdl(router_logits_split_kernel<TA, EP>, dim3(grid), dim3(256), 0, st,
         x, Wr, bias, logits, s.T, s.d, s.E, s.k, s.renorm ? 1 : 0, fused ? idx : nullptr,
         fused ? w : nullptr);
     return cudaGetLastError();
@@ -356,6 +358,7 @@ __global__ void __launch_bounds__(256)
 topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int nparts,
             const float *__restrict__ bias, int64_t T, int E, int k, int renorm,
             int32_t *__restrict__ idx, float *__restrict__ w) {
+    pdl_entry();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
@@ -448,7 +451,7 @@ template <int VPL>
 cudaError_t launch_topk_v(const Shape &s, float *logits, const float *partial, int nparts,
                           const float *bias, int32_t *idx, float *w, cudaStream_t st) {
     unsigned blocks = (unsigned)((s.T + 7) / 8);
-    topk_kernel<VPL><<<blocks, 256, 0, st>>>(logits, partial, nparts, bias, s.T, s.E, s.k,
+    launch_pdl(topk_kernel<VPL>, dim3(blocks), dim3(256), 0, st, logits, partial, nparts, bias, s.T, s.E, s.k,
                                              s.renorm ? 1 : 0, idx, w);
     return cudaGetLastError();
 }

@@ -73,6 +73,7 @@ inline RouterSmem router_smem(int E) {
 // the d columns, y over the experts (no integer division per element).
 __global__ void split_router_weight_kernel(const float *__restrict__ Wr, int d,
                                            __nv_bfloat16 *__restrict__ Wsplit) {
+    pdl_entry();
     const int e = blockIdx.y;
     const float *src = Wr + (int64_t)e * d;
     __nv_bfloat16 *row = Wsplit + (int64_t)e * 3 * d;
@@ -103,6 +104,7 @@ struct RouterParams {
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, RouterParams p) {
+    pdl_entry();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -294,8 +296,8 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
     __nv_bfloat16 *wsplit = static_cast<__nv_bfloat16 *>(scratch);
     float *partial = reinterpret_cast<float *>(static_cast<uint8_t *>(scratch) +
                                                (((size_t)s.E * 3 * s.d * 2 + 255) & ~(size_t)255));
-    split_router_weight_kernel<<<dim3((unsigned)std::min(8, (s.d + 255) / 256), (unsigned)s.E), 256, 0,
-                                 st>>>(Wr, s.d, wsplit);
+    launch_pdl(split_router_weight_kernel, dim3((unsigned)std::min(8, (s.d + 255) / 256), (unsigned)s.E), dim3(256), 0, st, Wr,
+               s.d, wsplit);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
 
     const RouterSmem m = router_smem(s.E);
@@ -323,7 +325,7 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
     p.tmem_cols = m.n_pad <= 32 ? 32 : m.n_pad <= 64 ? 64 : m.n_pad <= 128 ? 128 : 256;
     p.ds = ds;
     dim3 grid((unsigned)((s.T + RBM - 1) / RBM), (unsigned)pl.splits);
-    router_logits_tc_kernel<<<grid, R_THREADS, m.bytes, st>>>(mx, mw, p);
+    launch_pdl(router_logits_tc_kernel, dim3(grid), dim3(R_THREADS), m.bytes, st, mx, mw, p);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     *partial_out = partial;
     *splits_out = pl.splits;
