@@ -88,9 +88,13 @@ __device__ __forceinline__ void stg16(void *p, const uint4 &v) {
 // stream has completed and its writes are visible.  Nothing is read from
 // earlier kernels before that wait.  Launched without the attribute (or
 // after a copy), both instructions are no-ops.
-__device__ __forceinline__ void pdl_entry() {
+__device__ __forceinline__ void pdl_release() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_entry() {
+    pdl_release();
+    pdl_wait();
 }
 
 // Launch with programmatic stream serialization (see pdl_entry); extra

@@ -179,7 +179,7 @@ template <bool SWIGLU, int CTAS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, Params p) {
-    pdl_entry();
+    pdl_release();  // the wait for the previous kernel follows this CTA's own set-up
     using C = Cfg<CTAS>;
     constexpr bool PAIR = C::PAIR;
     constexpr int STAGES = C::STAGES;
@@ -208,8 +208,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t sig_full = PAIR ? map_to_rank(bar_full, 0) : bar_full;
     const uint32_t sig_tempty = PAIR ? map_to_rank(bar_tempty, 0) : bar_tempty;
 
-    // ---- prologue: row-tile prefix, barriers, tensor memory ----
-    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = p.offsets[e];
+    // ---- prologue: barriers and tensor memory, then (after the previous
+    // kernel has completed) the row-tile prefix from `offsets` ----
     if (threadIdx.x == 0) {
         *s_abort = 0;
         for (int i = 0; i < STAGES; ++i) {
@@ -225,6 +225,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) tmem_alloc<CTAS>(base_s + C::OFF_TMEM, TMEM_COLS);
+    pdl_wait();
+    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = p.offsets[e];
     __syncthreads();
     if (warp == 2) {  // prefix of ceil(count_e / TILE_M) over experts
         const int per = (E + 31) / 32;

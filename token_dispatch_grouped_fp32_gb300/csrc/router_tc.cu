@@ -104,7 +104,7 @@ struct RouterParams {
 __global__ void __launch_bounds__(R_THREADS, 1)
 router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                         const __grid_constant__ CUtensorMap tmW, RouterParams p) {
-    pdl_entry();
+    pdl_release();  // the wait for the weight split follows the set-up below
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -136,6 +136,7 @@ router_logits_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 0) tmem_alloc<1>(base_s + p.off_tmem, p.tmem_cols);
+    pdl_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
