@@ -10,6 +10,9 @@
 //   G1: h_perm[r] = silu(x_perm[r] @ Wgu[e][:, :f]) * (x_perm[r] @ Wgu[e][:, f:])
 //   G2: y_perm[r] = h_perm[r] @ Wd[e]
 // for every expert e and row r of its segment [offsets[e], offsets[e+1]).
+// The kernel's tile list is every G1 tile, then every G2 tile, and each
+// launch is given the column tiles of one product only (the other's count is
+// zero), so the product is a property of the tile, not of the template.
 //
 // Tiling.  Two tile shapes share one kernel template (CTAS = 1 or 2).
 //  - CTAS = 2 (a cluster of 2, tcgen05.mma.cta_group::2): the pair owns a
@@ -93,15 +96,20 @@ template <int CTAS> struct Cfg {
     static constexpr int EPI_ARRIVALS = 4 * CTAS;         // epilogue warps reporting per tile
 };
 
+// One product of the pair: [0] = G1 (gate/up + SwiGLU), [1] = G2 (down).
+struct PhaseParams {
+    int K;              // reduction length (d for G1, f for G2)
+    int n_out;          // output columns (f for G1, d for G2)
+    int n_tiles;        // column tiles per row tile
+    int transpose_epi;  // epilogue store pattern (see kTransposeMaxK)
+    __nv_bfloat16 *out;  // [P][n_out]
+};
+
 struct Params {
     const int32_t *offsets;
     int E;
-    int K;        // reduction length (d for G1, f for G2)
-    int n_out;    // output columns (f for G1, d for G2)
-    int f;        // column offset of the up half in Wgu (G1)
-    int n_tiles;  // column tiles per row tile
-    int transpose_epi;  // epilogue store pattern (see kTransposeMaxK)
-    __nv_bfloat16 *out;  // [P][n_out]
+    int f;              // column offset of the up half in Wgu
+    PhaseParams g1, g2;  // a launch runs one of them: the other has n_tiles = 0
     DevStatus ds;
 };
 
@@ -112,73 +120,86 @@ struct Params {
 // the epilogue warps.
 //
 // Epilogue store pattern (Params::transpose_epi): 0 = each thread stores its
-// own row (16-byte stores, 32 rows per warp instruction); 1 = 32 x 32 blocks
-// of packed bf16 pairs are transposed with shuffles so each warp instruction
-// stores 128 contiguous bytes of one row.  The second costs shuffles but
-// fewer memory transactions; it pays when epilogues are frequent relative to
-// the main loop (short K).
+// own row (16-byte stores, 32 rows per warp instruction); 1 = 16-byte chunks
+// are transposed with shuffles within groups of eight lanes so each warp
+// instruction stores 128 contiguous bytes of each of four rows.  The second
+// costs shuffles but fewer memory transactions; it pays when epilogues are
+// frequent relative to the main loop (short K).
 constexpr int kTransposeMaxK = 3072;
 
-// 32 x 32 transpose across the warp: before, lane l holds v[i] = M[l][i];
-// after, lane l holds v[i] = M[i][l].
-__device__ __forceinline__ void transpose32(uint32_t (&v)[32]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) {
-        const bool upper = (lane & s) != 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i & s) continue;
-            const uint32_t send = upper ? v[i] : v[i + s];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, s);
-            if (upper) v[i] = recv;
-            else v[i + s] = recv;
-        }
-    }
-}
-
 // Lane l holds packed[i] = bf16 pair (columns 2i, 2i+1 of a 64-column block)
-// of row (rbase + l).  Transpose so lane l holds pair l of rows rbase..+31 and
-// store each row's 128 bytes with one warp instruction.
+// of row (rbase + l): eight 16-byte chunks of 8 columns, chunk c in
+// packed[4c .. 4c+3].  An 8 x 8 transpose of the chunks within each group of
+// eight lanes (three butterfly steps over lane bits 4, 2, 1) leaves lane
+// 8g + j with chunk j of rows 8g .. 8g+7 in chunk slots 0..7, so each store
+// instruction writes 128 contiguous bytes of four rows: 48 shuffles and 8
+// 16-byte stores per block.
 __device__ __forceinline__ void store_rows_transposed(uint32_t (&packed)[32], __nv_bfloat16 *out,
                                                       int64_t rbase, int rows_valid, int col0,
                                                       int n_out) {
-    transpose32(packed);
     const int lane = threadIdx.x & 31;
-    const int col = col0 + 2 * lane;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (i < rows_valid && col + 2 <= n_out)
-            *reinterpret_cast<uint32_t *>(out + (rbase + i) * n_out + col) = packed[i];
+    for (int s = 4; s >= 1; s >>= 1) {
+        const bool upper = (lane & s) != 0;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (c & s) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t send = upper ? packed[4 * c + q] : packed[4 * (c + s) + q];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, s);
+                if (upper) packed[4 * c + q] = recv;
+                else packed[4 * (c + s) + q] = recv;
+            }
+        }
+    }
+    const int grp = lane >> 3;
+    const int col = col0 + 8 * (lane & 7);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 8 * grp + i;
+        if (r < rows_valid && col + 8 <= n_out)
+            stg16(out + (rbase + r) * n_out + col,
+                  make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
+    }
 }
 
 struct TileInfo {
     int e, row0, rows, n_blk;  // row0/rows: the tile's slice of expert e's segment
+    bool down;                 // a G2 tile
 };
 
-// Last e with s_tile[e] <= g, i.e. the expert whose row tiles hold g.
+// Tiles [0, total1) are G1 tiles, the rest G2 tiles; within each product the
+// order is expert, then column tile, then row tile.  The expert is the last e
+// with s_tile[e] <= (tile / column tiles).
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int *s_off, const int *s_tile,
-                                                int E, int n_tiles, int tile_m) {
-    const int g = tile / n_tiles;
+                                                int E, int total1, int n1, int n2, int tile_m) {
+    TileInfo ti;
+    ti.down = tile >= total1;
+    const int local = ti.down ? tile - total1 : tile;
+    const int n_tiles = ti.down ? n2 : n1;
+    const int g = local / n_tiles;
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
         if (s_tile[mid] <= g) lo = mid; else hi = mid - 1;
     }
-    TileInfo ti;
     ti.e = lo;
     const int mt = s_tile[lo + 1] - s_tile[lo];
-    const int r = tile - s_tile[lo] * n_tiles;
+    const int r = local - s_tile[lo] * n_tiles;
     ti.n_blk = r / mt;
     ti.row0 = s_off[lo] + (r % mt) * tile_m;
     ti.rows = min(tile_m, s_off[lo + 1] - ti.row0);
     return ti;
 }
 
-template <bool SWIGLU, int CTAS>
+// tmX / tmWgu: A and B of G1; tmH / tmWd: A and B of G2.
+template <int CTAS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, Params p) {
+grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmWgu,
+                       const __grid_constant__ CUtensorMap tmH,
+                       const __grid_constant__ CUtensorMap tmWd, Params p) {
     pdl_release();  // the wait for the previous kernel follows this CTA's own set-up
     using C = Cfg<CTAS>;
     constexpr bool PAIR = C::PAIR;
@@ -252,9 +273,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
     tc_fence_after();
 
     const uint32_t tmem_base = *s_tmem;
-    const int n_tiles = p.n_tiles;
-    const int total = s_tile[E] * n_tiles;
-    const int nk = (p.K + BK - 1) / BK;
+    const int n1 = p.g1.n_tiles, n2 = p.g2.n_tiles;
+    const int total1 = s_tile[E] * n1;
+    const int total = total1 + s_tile[E] * n2;
+    const int nk1 = (p.g1.K + BK - 1) / BK, nk2 = (p.g2.K + BK - 1) / BK;
 
     // The producer and the MMA issuer are single threads (lane 0 of warps 0
     // and 1): a warp-wide loop (a shuffle of each wait's result and a
@@ -268,13 +290,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             uint32_t issued = 0, last_par = 0;  // per stage armed here: ever / parity of last phase
             bool ok = true;
             for (int tile = unit; tile < total && ok; tile += nunits) {
-                const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles, C::TILE_M);
+                const TileInfo ti = decode_tile(tile, s_off, s_tile, E, total1, n1, n2, C::TILE_M);
+                const CUtensorMap *tmA = ti.down ? &tmH : &tmX;
+                const CUtensorMap *tmB = ti.down ? &tmWd : &tmWgu;
                 // first B column of this CTA: in G1 the gate columns come first and the
                 // up columns (offset f) follow; a pair splits them between its CTAs
                 int n0;
-                if (SWIGLU) n0 = ti.n_blk * (BN / 2) + (PAIR && !leader ? p.f : 0);
+                if (!ti.down) n0 = ti.n_blk * (BN / 2) + (PAIR && !leader ? p.f : 0);
                 else n0 = ti.n_blk * BN + (int)rank * (BN / 2);
                 const int arow = ti.row0 + (int)rank * BM;
+                const int nk = ti.down ? nk2 : nk1;
                 for (int ks = 0; ks < nk; ++ks) {
                     if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort)) {
                         ok = false;
@@ -287,13 +312,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                         issued |= 1u << s;
                         last_par = (last_par & ~(1u << s)) | (ph << s);
                     }
-                    tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, &tmA, k0, arow, fb);
+                    tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, tmA, k0, arow, fb);
                     const uint32_t bdst = base_s + C::OFF_B + s * C::B_BYTES;
 #pragma unroll
                     for (int a = 0; a < C::B_ATOMS; ++a) {
                         int col = n0 + 64 * a;
-                        if (SWIGLU && !PAIR && a >= 2) col = ti.n_blk * (BN / 2) + p.f + 64 * (a - 2);
-                        tma_load_3d<CTAS>(bdst + a * B_ATOM_BYTES, &tmB, col, k0, ti.e, fb);
+                        if (!PAIR && !ti.down && a >= 2) col = ti.n_blk * (BN / 2) + p.f + 64 * (a - 2);
+                        tma_load_3d<CTAS>(bdst + a * B_ATOM_BYTES, tmB, col, k0, ti.e, fb);
                     }
                     if (++s == STAGES) {
                         s = 0;
@@ -338,6 +363,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int tile = unit; tile < total && ok; tile += nunits, ++it) {
                 const int acc = it & 1;
                 const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+                const int nk = tile < total1 ? nk1 : nk2;
                 if (!wait_bounded(bar_tempty + 8 * acc, aph ^ 1u, p.ds, s_abort)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -375,7 +401,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
         const int r_in_tile = (int)rank * BM + quarter * 32 + lane;
         int it = 0;
         for (int tile = unit; tile < total; tile += nunits, ++it) {
-            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, n_tiles, C::TILE_M);
+            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, total1, n1, n2, C::TILE_M);
+            const bool sw = !ti.down;  // G1: SwiGLU of the gate and up halves
+            __nv_bfloat16 *const out = sw ? p.g1.out : p.g2.out;
+            const int n_out = sw ? p.g1.n_out : p.g2.n_out;
+            const int transpose = sw ? p.g1.transpose_epi : p.g2.transpose_epi;
             const int acc = it & 1;
             const uint32_t aph = (uint32_t)(it >> 1) & 1u;
             const int good = __all_sync(0xffffffffu,
@@ -384,18 +414,18 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
             tc_fence_after();
             const uint32_t t_row = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
             const bool row_ok = r_in_tile < ti.rows;
-            __nv_bfloat16 *orow = p.out + (int64_t)(ti.row0 + r_in_tile) * p.n_out;
-            if (p.transpose_epi) {
+            __nv_bfloat16 *orow = out + (int64_t)(ti.row0 + r_in_tile) * n_out;
+            if (transpose) {
                 // rows of this warp: ti.row0 + rank*BM + quarter*32 + (0..31)
                 const int wrow0 = (int)rank * BM + quarter * 32;
                 const int rows_valid = max(0, min(32, ti.rows - wrow0));
                 const int64_t rbase = (int64_t)ti.row0 + wrow0;
-                const int ncols = SWIGLU ? BN / 2 : BN;
+                const int ncols = sw ? BN / 2 : BN;
                 const int n0 = ti.n_blk * ncols;
 #pragma unroll 1
                 for (int c = 0; c < ncols; c += 64) {
                     uint32_t packed[32];
-                    if (SWIGLU) {
+                    if (sw) {
 #pragma unroll
                         for (int half = 0; half < 2; ++half) {
                             uint32_t g[32], u[32];
@@ -425,9 +455,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                             }
                         }
                     }
-                    store_rows_transposed(packed, p.out, rbase, rows_valid, n0 + c, p.n_out);
+                    store_rows_transposed(packed, out, rbase, rows_valid, n0 + c, n_out);
                 }
-            } else if (SWIGLU) {
+            } else if (sw) {
                 const int n0 = ti.n_blk * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
@@ -449,7 +479,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             const int col = n0 + c + 8 * v;
-                            if (col + 8 <= p.n_out)
+                            if (col + 8 <= n_out)
                                 stg16(orow + col, make_uint4(packed[4 * v], packed[4 * v + 1],
                                                              packed[4 * v + 2], packed[4 * v + 3]));
                         }
@@ -473,7 +503,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
                             const int col = n0 + c + 8 * v;
-                            if (col + 8 <= p.n_out)
+                            if (col + 8 <= n_out)
                                 stg16(orow + col, make_uint4(packed[4 * v], packed[4 * v + 1],
                                                              packed[4 * v + 2], packed[4 * v + 3]));
                         }
@@ -521,60 +551,67 @@ cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttri
     return cfg;
 }
 
-template <bool SWIGLU, int CTAS>
-cudaError_t launch(unsigned grid, const CUtensorMap &ta, const CUtensorMap &tb, const Params &p,
+template <int CTAS>
+cudaError_t launch(unsigned grid, const CUtensorMap &mx, const CUtensorMap &mwgu,
+                   const CUtensorMap &mh, const CUtensorMap &mwd, const Params &p,
                    cudaStream_t st) {
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<CTAS>(grid, st, attr);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<SWIGLU, CTAS>, ta, tb, p);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS>, mx, mwgu, mh, mwd, p);
 }
 
-template <bool SWIGLU, int CTAS> cudaError_t prepare(int *resident_units) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<SWIGLU, CTAS>,
+template <int CTAS> cudaError_t prepare(int *resident_units) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            Cfg<CTAS>::SMEM_BYTES);
     if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<CTAS>(CTAS, nullptr, attr);
-    return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<SWIGLU, CTAS>,
-                                          &cfg);
+    return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<CTAS>, &cfg);
 }
+
+// Upper bound of the row tiles: sum_e ceil(count_e/TM) <= P/TM + min(E, P).
+int64_t row_tiles_bound(const Shape &s, int tile_m) {
+    const int64_t P = s.P();
+    return (P + tile_m - 1) / tile_m + std::min<int64_t>(s.E, P);
+}
+
+bool use_pairs(const Shape &s) { return s.P() >= (int64_t)kPairRowsPerExpert * s.E; }
 
 template <int CTAS>
 cudaError_t run(const Shape &s, int units, const CUtensorMap &mx, const CUtensorMap &mwgu,
                 const CUtensorMap &mh, const CUtensorMap &mwd, const int32_t *offsets,
                 void *h_perm, void *y_perm, const DevStatus &ds, cudaStream_t st) {
-    const int64_t P = s.P();
-    constexpr int TM = Cfg<CTAS>::TILE_M;
-    // Upper bound of the row tiles: sum_e ceil(count_e/TM) <= P/TM + min(E, P).
-    const int64_t row_tiles_max = (P + TM - 1) / TM + std::min<int64_t>(s.E, P);
+    const int64_t row_tiles_max = row_tiles_bound(s, Cfg<CTAS>::TILE_M);
     const int64_t n_tiles1 = (s.f + BN / 2 - 1) / (BN / 2), n_tiles2 = (s.d + BN - 1) / BN;
-    if (row_tiles_max * std::max(n_tiles1, n_tiles2) >= (int64_t)INT32_MAX) {
+    if (row_tiles_max * (n_tiles1 + n_tiles2) >= (int64_t)INT32_MAX) {
         set_error_message("grouped GEMM tile count exceeds 2^31");
         return cudaErrorInvalidValue;
     }
-    Params p1;
-    p1.offsets = offsets;
-    p1.E = s.E;
-    p1.K = s.d;
-    p1.n_out = s.f;
-    p1.f = s.f;
-    p1.n_tiles = (int)n_tiles1;
-    p1.transpose_epi = s.d <= kTransposeMaxK;
-    p1.out = static_cast<__nv_bfloat16 *>(h_perm);
-    p1.ds = ds;
-    const unsigned g1 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles1);
-    cudaError_t err = launch<true, CTAS>(g1, mx, mwgu, p1, st);
+    Params p;
+    p.offsets = offsets;
+    p.E = s.E;
+    p.f = s.f;
+    p.g1.K = s.d;
+    p.g1.n_out = s.f;
+    p.g1.n_tiles = (int)n_tiles1;
+    p.g1.transpose_epi = s.d <= kTransposeMaxK;
+    p.g1.out = static_cast<__nv_bfloat16 *>(h_perm);
+    p.g2.K = s.f;
+    p.g2.n_out = s.d;
+    p.g2.n_tiles = (int)n_tiles2;
+    p.g2.transpose_epi = s.f <= kTransposeMaxK;
+    p.g2.out = static_cast<__nv_bfloat16 *>(y_perm);
+    p.ds = ds;
+    // G1 tiles only, then G2 tiles only (the second launch reads h_perm)
+    Params p1 = p, p2 = p;
+    p1.g2.n_tiles = 0;
+    p2.g1.n_tiles = 0;
+    const unsigned grid1 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles1);
+    const unsigned grid2 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles2);
+    cudaError_t err = launch<CTAS>(grid1, mx, mwgu, mh, mwd, p1, st);
     if (err != cudaSuccess) return err;
-    Params p2 = p1;
-    p2.K = s.f;
-    p2.n_out = s.d;
-    p2.f = 0;
-    p2.n_tiles = (int)n_tiles2;
-    p2.transpose_epi = s.f <= kTransposeMaxK;
-    p2.out = static_cast<__nv_bfloat16 *>(y_perm);
-    const unsigned g2 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles2);
-    return launch<false, CTAS>(g2, mh, mwd, p2, st);
+    return launch<CTAS>(grid2, mx, mwgu, mh, mwd, p2, st);
 }
 
 }  // namespace tc
@@ -589,12 +626,11 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!info[dev].ready) {
-        int a = 0, b = 0, c = 0, d = 0;
-        if ((err = prepare<true, 1>(&a)) != cudaSuccess || (err = prepare<false, 1>(&b)) != cudaSuccess ||
-            (err = prepare<true, 2>(&c)) != cudaSuccess || (err = prepare<false, 2>(&d)) != cudaSuccess)
+        int a = 0, c = 0;
+        if ((err = prepare<1>(&a)) != cudaSuccess || (err = prepare<2>(&c)) != cudaSuccess)
             return err;
-        info[dev].sms = std::min(a, b);
-        info[dev].pairs = std::min(c, d);
+        info[dev].sms = a;
+        info[dev].pairs = c;
         if (info[dev].sms < 1 || info[dev].pairs < 1) {
             set_error_message("the grouped GEMM does not fit on device %d", dev);
             return cudaErrorInvalidConfiguration;
@@ -615,7 +651,7 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     }
     // Pairs (256-row tiles) when experts average >= 512 rows; else 128-row
     // tiles, which waste less on ragged segments and small batches.
-    if (P >= (int64_t)kPairRowsPerExpert * s.E)
+    if (use_pairs(s))
         return run<2>(s, info[dev].pairs, mx, mwgu, mh, mwd, offsets, h_perm, y_perm, ds, st);
     return run<1>(s, info[dev].sms, mx, mwgu, mh, mwd, offsets, h_perm, y_perm, ds, st);
 }
