@@ -65,15 +65,14 @@ def test_cuda_graph_capture(moe):
     layer, x = _layer(moe, "gptoss_prefill", 1000)
     ref = layer(x).clone()
     out = torch.empty_like(x)
-    layer.workspace(x.shape[0])
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        layer(x, out=out)  # warm up on the capture stream
+        layer(x, out=out)  # warm up on the capture stream (allocates its workspace)
     torch.cuda.current_stream().wait_stream(s)
     g = torch.cuda.CUDAGraph()
     out.zero_()
-    with torch.cuda.graph(g):
+    with torch.cuda.graph(g, stream=s):
         layer(x, out=out)
     g.replay()
     torch.cuda.synchronize()
@@ -92,3 +91,23 @@ def test_forward_host_buffers(moe):
                          out_host, x_dev, out_dev, layer.workspace(x.shape[0]))
     torch.cuda.synchronize()
     assert torch.equal(out_host, ref.cpu())
+
+
+def test_concurrent_streams_have_their_own_workspace(moe):
+    """Two calls in flight on two streams: each stream gets its own workspace
+    from MoELayer, and both outputs equal the serial result."""
+    layer, x = _layer(moe, "qwen3_zipf", 2048)
+    ref = layer(x).clone()
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    T = x.shape[0]
+    assert layer.workspace(T, streams[0]).data_ptr() != layer.workspace(T, streams[1]).data_ptr()
+    outs = [torch.empty_like(x) for _ in streams]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    for _ in range(4):  # interleaved, so the two streams' kernels overlap
+        for st, o in zip(streams, outs):
+            layer(x, out=o, stream=st)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, ref)

@@ -6,8 +6,8 @@ argument order.  All arithmetic runs in libmoe's CUDA kernels; if the library
 is missing this module raises at import time instead of falling back to
 anything else.
 
-``MoELayer`` is a small convenience holder: it keeps the weights and a
-workspace (allocated with torch) and calls ``moe_forward``.
+``MoELayer`` is a small convenience holder: it keeps the weights and one
+workspace per stream (allocated with torch) and calls ``moe_forward``.
 """
 from __future__ import annotations
 
@@ -215,10 +215,14 @@ def moe_last_device_error(stream=None, raise_on_error=True):
 
 
 class MoELayer:
-    """Weights of one MoE layer plus a reusable workspace; ``forward`` runs
-    ``moe_forward`` on the current stream.  Weights: Wr [E, d] fp32,
-    W_gate_up [E, d, 2f] and W_down [E, f, d] in the activation dtype,
-    optional per-expert logit bias [E] fp32."""
+    """Weights of one MoE layer plus reusable workspaces; ``forward`` runs
+    ``moe_forward`` on the given (default: current) stream.  Weights: Wr [E, d]
+    fp32, W_gate_up [E, d, 2f] and W_down [E, f, d] in the activation dtype,
+    optional per-expert logit bias [E] fp32.
+
+    The workspace holds a call's intermediates (logits, routing, permuted
+    rows), so two calls in flight at once must not share one: the layer keeps
+    a separate workspace for each stream it is called on."""
 
     def __init__(self, Wr, W_gate_up, W_down, k, logit_bias=None, renormalize=True,
                  scale_inputs=False):
@@ -230,17 +234,22 @@ class MoELayer:
         self.dtype = W_gate_up.dtype
         self.renormalize = renormalize
         self.scale_inputs = scale_inputs
-        self._ws = None
+        self._ws = {}  # stream handle -> workspace
 
     def config(self, T: int) -> moe_config_t:
         return config(T, self.d, self.E, self.k, self.f, self.dtype, self.renormalize,
                       self.scale_inputs)
 
-    def workspace(self, T: int):
+    def workspace(self, T: int, stream=None):
+        """The workspace for calls on `stream` (default: the current stream),
+        grown to moe_workspace_size for T tokens when needed."""
+        key = _stream(stream).value or 0
         need = moe_workspace_size(self.config(T))
-        if self._ws is None or self._ws.numel() < need:
-            self._ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.Wr.device)
-        return self._ws
+        ws = self._ws.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=self.Wr.device)
+            self._ws[key] = ws
+        return ws
 
     def forward(self, x, out=None, stream=None):
         T = x.shape[0]
@@ -248,7 +257,7 @@ class MoELayer:
             out = torch.empty_like(x)
         cfg = self.config(T)
         moe_forward(cfg, x, self.Wr, self.logit_bias, self.W_gate_up, self.W_down, out,
-                    self.workspace(T), stream=stream)
+                    self.workspace(T, stream), stream=stream)
         return out
 
     __call__ = forward
