@@ -90,8 +90,11 @@ def test_route_logits_and_selection(moe, oracle, name, T):
     assert len(differ) <= max(2, T // 200)
 
 
-# Tensor-core logit shapes: N = E rounded up to 16, three W' tiles per stage
-# for N <= 128 (x read once), one per stage above; row tiles ragged at T.
+# Tensor-core logit shapes: N = E rounded up to 16.  Single CTAs (E < 64 or
+# T < 512): three W' tiles per stage for N <= 128 (x read once), one per
+# stage above.  CTA pairs (E >= 64, T >= 512): 256-token tiles, each CTA with
+# half of the N rows of every W' term; N = 64 ... 256, ragged token tiles
+# (the peer CTA's rows past T), W' rows past E, one or several K splits.
 TC_SHAPES = [
     # T, d, E, k
     (1024, 256, 8, 2),
@@ -101,6 +104,13 @@ TC_SHAPES = [
     (1024, 64, 64, 8),
     (1030, 192, 136, 4),
     (1024, 64, 256, 8),
+    (513, 256, 128, 8),     # pairs: 3 tiles, the last with one token; 2 K splits
+    (777, 256, 128, 4),
+    (1300, 192, 96, 4),     # N = 96: 48 W' rows per CTA
+    (600, 128, 200, 8),     # N = 208: the peer's rows 200..207 read zeros
+    (2048, 2048, 128, 8),   # 8 K splits
+    (4096, 512, 256, 8),    # N = 256, 4 K splits
+    (300, 448, 256, 8),     # T < 512: single CTAs, one W' tile per stage
 ]
 
 

@@ -35,6 +35,7 @@ cudaError_t launch_topk_partials(const Shape &s, const float *partial, int split
 
 // Router logits on the tensor cores (bf16 x, fp32 Wr split into 3 bf16 terms).
 struct RouterTcPlan {
+    int ctas;          // 2: CTA pairs on 256-token tiles; 1: single CTAs on 128-token tiles
     int ks_total;      // pipeline stages of a row tile: d / 64 (three W' tiles each) or 3d / 64
     int ks_per_split;  // stages per CTA
     int splits;        // K splits (blockIdx.y)

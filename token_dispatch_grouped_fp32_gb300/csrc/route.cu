@@ -323,31 +323,26 @@ cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const 
 // ---------------------------------------------------------------------------
 // Top-k: one warp per token.  Lane l holds logits l, l+32, ...; k rounds of a
 // warp arg-max under the rank order pick the experts; slot j is written by
-// lane j.  Weights: softmax over all E logits (max-shifted), then optional
+// lane j.  Each round is two warp reductions (redux.sync): the maximum of the
+// values' order-preserving 32-bit images, then the minimum expert id among
+// the still-available values that reach it (the lower id wins ties).
+// Weights: softmax over all E logits (max-shifted), then optional
 // renormalisation over the chosen k.
 // ---------------------------------------------------------------------------
 
 constexpr int kNoExpert = 0x7fffffff;
 
-// The rank order as one unsigned 64-bit key: an order-preserving image of
-// the float in the high word (+0.0 and -0.0 alike, a NaN lowest) and the
-// complement of the expert id in the low word (so the lower id wins ties).
-// key(a, ia) > key(b, ib) exactly when ranks_before(a, ia, b, ib); 0 means
-// "no candidate".
-__device__ __forceinline__ unsigned long long select_key(float v, int e) {
-    uint32_t o = 0u;
-    if (!isnan(v)) {
-        const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
-        o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    }
-    return ((unsigned long long)o << 32) | (0xFFFFFFFFu - (uint32_t)e);
+// Order-preserving unsigned image of a logit: a > b as floats exactly when
+// rank_bits(a) > rank_bits(b), with +0.0 and -0.0 alike and a NaN lowest (0;
+// no number maps to 0).  With the lower expert id breaking ties this is the
+// order ranks_before defines.
+__device__ __forceinline__ uint32_t rank_bits(float v) {
+    if (isnan(v)) return 0u;
+    const uint32_t b = __float_as_uint(v == 0.f ? 0.f : v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
-__device__ __forceinline__ float key_value(unsigned long long key) {
-    const uint32_t o = (uint32_t)(key >> 32);
+__device__ __forceinline__ float rank_value(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
-}
-__device__ __forceinline__ int key_expert(unsigned long long key) {
-    return (int)(0xFFFFFFFFu - (uint32_t)key);
 }
 
 // With nparts > 0 the logits are first formed as the sum of nparts partial
@@ -399,35 +394,35 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
     for (int i = 0; i < VPL; ++i)
         if (!((avail >> i) & 1u)) v[i] = -INFINITY;
 
-    unsigned long long key[VPL];
+    uint32_t ord[VPL];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) key[i] = select_key(v[i], lane + 32 * i);
+    for (int i = 0; i < VPL; ++i) ord[i] = rank_bits(v[i]);
     float my_v = 0.f;
     int my_e = 0;
+    uint32_t top = 0u;  // the first round's maximum: the largest logit
     for (int j = 0; j < k; ++j) {
-        unsigned long long best = 0ull;
+        // every round has an available value somewhere in the warp (j < k <= E)
+        uint32_t lmax = 0u;
 #pragma unroll
         for (int i = 0; i < VPL; ++i)
-            if ((avail >> i) & 1u) best = key[i] > best ? key[i] : best;
+            if ((avail >> i) & 1u) lmax = ord[i] > lmax ? ord[i] : lmax;
+        const uint32_t omax = __reduce_max_sync(0xffffffffu, lmax);
+        uint32_t le = 0xFFFFFFFFu;  // this lane's lowest available expert at the maximum
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
-        }
-        const int be = key_expert(best);
+        for (int i = VPL - 1; i >= 0; --i)
+            if (((avail >> i) & 1u) && ord[i] == omax) le = (uint32_t)(lane + 32 * i);
+        const int be = (int)__reduce_min_sync(0xffffffffu, le);
         if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+        if (j == 0) top = omax;
         if (lane == j) {
-            my_v = key_value(best);
+            my_v = rank_value(omax);
             my_e = be;
         }
     }
 
-    // softmax over all E logits
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) m = fmaxf(m, v[i]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    // softmax over all E logits, shifted by their maximum (-inf if every
+    // logit is NaN, as a max that skips NaNs would give)
+    const float m = top != 0u ? rank_value(top) : -INFINITY;
     float z = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) z += expf(v[i] - m);
