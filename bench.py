@@ -344,7 +344,11 @@ def run_ours(args, w):
     es = 2 if w.dtype == "bf16" else 4
     gemm_flops = 6.0 * P * w.d * w.f
     gemm_tflops = gemm_flops / (kms["grouped_swiglu"] * 1e-3) / 1e12
-    # minimal HBM bytes of the bandwidth kernels
+    # minimal HBM bytes of the bandwidth kernels: dispatch reads each token row
+    # once and writes each permuted row once (+ four int32 arrays of P);
+    # combine reads the permuted rows and the (pos, weight) pairs and writes
+    # the token rows; route reads x and writes the logits twice (partial sums
+    # and the final logits) plus the selection
     disp_bytes = T * w.d * es + P * w.d * es + P * 4 * 4
     comb_bytes = P * w.d * es + P * 8 + T * w.d * es
     route_bytes = T * w.d * es + T * w.E * 4 * 2 + P * 8
