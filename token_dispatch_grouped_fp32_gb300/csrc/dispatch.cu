@@ -30,6 +30,7 @@ chunk_histogram_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int ch
     __syncthreads();
     const int64_t q0 = (int64_t)blockIdx.x * chunk;
     const int64_t q1 = min(q0 + chunk, P);
+#pragma unroll 8  // independent iterations: several index loads in flight
     for (int64_t q = q0 + threadIdx.x; q < q1; q += kThreads) {
         int e = idx[q];
         if ((unsigned)e < (unsigned)E)
@@ -42,15 +43,28 @@ chunk_histogram_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int ch
 }
 
 // Single block: exclusive scan of hist[0 .. E*NB) in place (the base row of
-// every (expert, chunk)), then counts[e] and offsets[0..E].
+// every (expert, chunk)), then counts[e] and offsets[0..E].  STAGED: the
+// matrix (at most kScanStageMax ints) is first copied to shared memory with
+// coalesced loads, scanned there and copied back, so each thread's serial
+// walk over its segment reads shared memory instead of waiting on one global
+// load after another.
 constexpr int kScanThreads = 1024;
+constexpr int kScanStageMax = 12 * 1024 - 64;  // ints: with the static arrays, under 48 KB
+template <bool STAGED>
 __global__ void __launch_bounds__(kScanThreads)
-scan_kernel(int32_t *__restrict__ hist, int E, int NB, int32_t *__restrict__ counts,
+scan_kernel(int32_t *__restrict__ hist_g, int E, int NB, int32_t *__restrict__ counts,
             int32_t *__restrict__ offsets) {
     pdl_entry();
     __shared__ int warp_tot[kScanThreads / 32];
     __shared__ int total_s;
+    extern __shared__ int sh_hist[];
     const int n = E * NB;
+    int32_t *hist = hist_g;
+    if (STAGED) {
+        for (int i = threadIdx.x; i < n; i += kScanThreads) sh_hist[i] = hist_g[i];
+        __syncthreads();
+        hist = sh_hist;
+    }
     const int seg = (n + kScanThreads - 1) / kScanThreads;
     const int beg = min(n, (int)threadIdx.x * seg);
     const int end = min(n, beg + seg);
@@ -85,6 +99,8 @@ scan_kernel(int32_t *__restrict__ hist, int E, int NB, int32_t *__restrict__ cou
         run += c;
     }
     __syncthreads();
+    if (STAGED)
+        for (int i = threadIdx.x; i < n; i += kScanThreads) hist_g[i] = sh_hist[i];
     const int total = total_s;
     for (int e = threadIdx.x; e < E; e += kScanThreads) {
         int b0 = hist[e * NB];
@@ -109,6 +125,7 @@ scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chu
     const int64_t w0 = (int64_t)blockIdx.x * chunk + (int64_t)wid * sub;
     const int64_t w1 = min(w0 + sub, P);
     int *mine = sh_warp + wid * E;
+#pragma unroll 8  // independent iterations: several index loads in flight
     for (int64_t q = w0 + lane; q < w1; q += 32) {
         int e = idx[q];
         if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
@@ -124,13 +141,13 @@ scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chu
     }
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
+    // the next iteration's expert id is loaded before this one is ranked
+    int e_next = (w0 + lane < w1) ? idx[w0 + lane] : -1;
     for (int64_t qb = w0; qb < w1; qb += 32) {  // warp-uniform trip count
         const int64_t q = qb + lane;
-        int e = -1;
-        if (q < w1) {
-            e = idx[q];
-            if ((unsigned)e >= (unsigned)E) e = -1;
-        }
+        int e = e_next;
+        if (q < w1 && (unsigned)e >= (unsigned)E) e = -1;
+        e_next = (q + 32 < w1) ? idx[q + 32] : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(peers & lt_mask);
         const int row0 = (e >= 0) ? mine[e] : 0;
@@ -236,7 +253,13 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
                                                                         g.blocks, hist, ds);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    launch_pdl(scan_kernel, dim3(1), dim3(kScanThreads), 0, st, hist, s.E, g.blocks, counts, offsets);
+    const int64_t n_hist = (int64_t)s.E * g.blocks;
+    if (n_hist <= kScanStageMax)
+        launch_pdl(scan_kernel<true>, dim3(1), dim3(kScanThreads), sizeof(int) * (size_t)n_hist, st,
+                   hist, s.E, g.blocks, counts, offsets);
+    else
+        launch_pdl(scan_kernel<false>, dim3(1), dim3(kScanThreads), 0, st, hist, s.E, g.blocks,
+                   counts, offsets);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     const size_t sh = sizeof(int) * (size_t)kWarps * s.E;
     launch_pdl(scatter_kernel, dim3(g.blocks), dim3(kThreads), sh, st, idx, P, s.k, s.E, g.chunk, g.blocks, hist, pos,
