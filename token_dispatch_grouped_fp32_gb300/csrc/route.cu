@@ -57,6 +57,8 @@ __device__ __forceinline__ void warp_reduce_scatter32(float (&v)[32]) {
 
 constexpr int kSplitWarps = 8;
 
+constexpr int kNoExpert = 0x7fffffff;  // "no candidate" in a warp arg-max
+
 // Rank order of the selection: a larger logit first; equal logits (+0.0 and
 // -0.0 are equal) to the lower expert id; a NaN below every number.
 __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
@@ -147,12 +149,12 @@ router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ W
             int my_e = 0;
             for (int j = 0; j < k; ++j) {
                 float bv = avail ? v : NAN;
-                int be = avail ? e : 0x7fffffff;
+                int be = avail ? e : kNoExpert;
 #pragma unroll
                 for (int off = EP / 2; off > 0; off >>= 1) {
                     const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
                     const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                    if (oe != 0x7fffffff && (be == 0x7fffffff || ranks_before(ov, oe, bv, be))) {
+                    if (oe != kNoExpert && (be == kNoExpert || ranks_before(ov, oe, bv, be))) {
                         bv = ov;
                         be = oe;
                     }
@@ -329,8 +331,6 @@ cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const 
 // Weights: softmax over all E logits (max-shifted), then optional
 // renormalisation over the chosen k.
 // ---------------------------------------------------------------------------
-
-constexpr int kNoExpert = 0x7fffffff;
 
 // Order-preserving unsigned image of a logit: a > b as floats exactly when
 // rank_bits(a) > rank_bits(b), with +0.0 and -0.0 alike and a NaN lowest (0;
