@@ -150,6 +150,9 @@ def test_forward_kernel_launches(moe):
     # Mixtral-shaped, bf16, E = 8, T = 4096: tensor-core router (weight split,
     # logits, top-k) + dispatch (4) + G1, G2 + combine
     assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 10
+    # about 256 rows per expert: G1 and G2 each as a CTA-pair launch and a
+    # single-CTA launch, the experts split between them
+    assert moe.moe_forward_kernel_launches(moe.config(8192, 2880, 128, 4, 2880, "bf16")) == 12
     # small batch, E <= 32: logits and selection in one CUDA-core launch
     assert moe.moe_forward_kernel_launches(moe.config(64, 128, 8, 2, 256, "f32")) == 8
     # fp32 activations, E > 32: CUDA-core logits, then the top-k kernel

@@ -1,8 +1,9 @@
 """Grouped SwiGLU parity: h_perm and y_perm of every row against the oracle's
 expert FFN, for ragged segments (empty experts, partial row tiles, partial
 column tiles and a partial K step), with both tile shapes: 128-row tiles on
-one CTA (small per-expert batches) and 256-row tiles on a CTA pair (batches
-averaging >= 512 rows per expert)."""
+one CTA (small per-expert batches), 256-row tiles on a CTA pair (batches
+averaging >= 512 rows per expert), and in between each expert on the shape
+that pads it less."""
 import numpy as np
 import pytest
 import torch
@@ -37,6 +38,10 @@ EXPERT_CASES = [
     # CTA pairs whose experts end in short row tiles (76, 108, 176 rows; 128, 129, 1)
     ([1100, 620, 1200, 0], 200, 328),
     ([128, 129, 1, 1800], 72, 136),
+    # 64..511 rows per expert on average: each expert on the tile shape that pads
+    # it less (256-row pairs for 129..256 rows, 128-row single CTAs for 300)
+    ([200, 256, 129, 250], 128, 256),   # every expert on pairs: the single-CTA launch is empty
+    ([300, 129, 64, 256, 1], 192, 136), # both launches busy
 ]
 
 

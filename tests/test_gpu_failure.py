@@ -7,8 +7,9 @@ the device error word, the other roles give up at their next wait, the
 producers wait for the copies they issued (a 1 s floor), the tensor memory is
 freed and the kernel returns.  The host reads the status; the context stays
 usable and the next call (hook off, default limit) is bit-identical to one
-made before.  No trap, fault or hang is involved.  Both tile shapes are
-covered: CTA pairs (Mixtral-shaped, >= 512 rows per expert) and single CTAs."""
+made before.  No trap, fault or hang is involved.  Every tile mode is
+covered: CTA pairs (Mixtral-shaped, >= 512 rows per expert), single CTAs, and
+the experts split between the two (about 128 rows per expert)."""
 import pytest
 import torch
 
@@ -23,7 +24,8 @@ def moe():
     return load_moe()
 
 
-@pytest.mark.parametrize("name,T", [("mixtral", 4096), ("gptoss_prefill", 512)])
+@pytest.mark.parametrize("name,T", [("mixtral", 4096), ("gptoss_prefill", 512),
+                                    ("gptoss_prefill", 4096)])  # pairs; single CTAs; both
 def test_wait_timeout_is_reported_and_recoverable(moe, name, T):
     w = synth.WORKLOADS[name].with_tokens(T)
     inp = synth.make_inputs(w, device="cuda")

@@ -110,6 +110,7 @@ struct Params {
     int E;
     int f;              // column offset of the up half in Wgu
     PhaseParams g1, g2;  // a launch runs one of them: the other has n_tiles = 0
+    int experts;  // which experts this launch serves: kAllExperts, kPairExperts, kSingleExperts
     DevStatus ds;
 };
 
@@ -162,6 +163,21 @@ __device__ __forceinline__ void store_rows_transposed(uint32_t (&packed)[32], __
             stg16(out + (rbase + r) * n_out + col,
                   make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]));
     }
+}
+
+// Experts split between the two tile shapes by row count: CTA-pair tiles
+// (256 rows) serve an expert when they pad its rows to no more than 1.16x
+// what 128-row single-CTA tiles would (the single tile's cost per MMA row,
+// measured, from its larger shared-memory fill per SM).  The predicate is
+// evaluated on the device from `offsets`, identically by both launches.
+constexpr int kAllExperts = 0, kPairExperts = 1, kSingleExperts = 2;
+__host__ __device__ __forceinline__ bool pair_tiles_pay(int count) {
+    const int pair_rows = (count + 255) / 256 * 256, single_rows = (count + 127) / 128 * 128;
+    return pair_rows * 100 <= single_rows * 116;
+}
+__device__ __forceinline__ int expert_row_tiles(int count, int tile_m, int experts) {
+    if (experts != kAllExperts && pair_tiles_pay(count) != (experts == kPairExperts)) return 0;
+    return (count + tile_m - 1) / tile_m;
 }
 
 struct TileInfo {
@@ -249,11 +265,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     pdl_wait();
     for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = p.offsets[e];
     __syncthreads();
-    if (warp == 2) {  // prefix of ceil(count_e / TILE_M) over experts
+    if (warp == 2) {  // prefix over experts of their row tiles in this launch
         const int per = (E + 31) / 32;
         const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
         int local = 0;
-        for (int e = e0; e < e1; ++e) local += (s_off[e + 1] - s_off[e] + C::TILE_M - 1) / C::TILE_M;
+        for (int e = e0; e < e1; ++e) local += expert_row_tiles(s_off[e + 1] - s_off[e], C::TILE_M, p.experts);
         int incl = local;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -263,7 +279,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         int run = incl - local;
         for (int e = e0; e < e1; ++e) {
             s_tile[e] = run;
-            run += (s_off[e + 1] - s_off[e] + C::TILE_M - 1) / C::TILE_M;
+            run += expert_row_tiles(s_off[e + 1] - s_off[e], C::TILE_M, p.experts);
         }
         if (lane == 31) s_tile[E] = incl;
     }
@@ -576,45 +592,40 @@ int64_t row_tiles_bound(const Shape &s, int tile_m) {
     return (P + tile_m - 1) / tile_m + std::min<int64_t>(s.E, P);
 }
 
-bool use_pairs(const Shape &s) { return s.P() >= (int64_t)kPairRowsPerExpert * s.E; }
+// Tile shapes of a call.  Pairs when experts average >= 512 rows; 128-row
+// single-CTA tiles for small per-expert batches (decode); in between, each
+// expert goes to the shape that pads it less (pair_tiles_pay), in two
+// launches per product.
+enum TileMode { kModePairs, kModeHybrid, kModeSingles };
+constexpr int kHybridRowsPerExpert = 64;  // below this average: single-CTA tiles only
+TileMode tile_mode(const Shape &s) {
+    if (s.P() >= (int64_t)kPairRowsPerExpert * s.E) return kModePairs;
+    if (s.P() >= (int64_t)kHybridRowsPerExpert * s.E) return kModeHybrid;
+    return kModeSingles;
+}
 
+// The launch of one product (G1: phase 1, G2: phase 2) over the experts
+// `experts` selects, with one tile shape.
 template <int CTAS>
-cudaError_t run(const Shape &s, int units, const CUtensorMap &mx, const CUtensorMap &mwgu,
-                const CUtensorMap &mh, const CUtensorMap &mwd, const int32_t *offsets,
-                void *h_perm, void *y_perm, const DevStatus &ds, cudaStream_t st) {
+cudaError_t launch_product(const Shape &s, int units, const CUtensorMap &mx,
+                           const CUtensorMap &mwgu, const CUtensorMap &mh,
+                           const CUtensorMap &mwd, const Params &both, int phase, int experts,
+                           cudaStream_t st) {
     const int64_t row_tiles_max = row_tiles_bound(s, Cfg<CTAS>::TILE_M);
-    const int64_t n_tiles1 = (s.f + BN / 2 - 1) / (BN / 2), n_tiles2 = (s.d + BN - 1) / BN;
-    if (row_tiles_max * (n_tiles1 + n_tiles2) >= (int64_t)INT32_MAX) {
-        set_error_message("grouped GEMM tile count exceeds 2^31");
-        return cudaErrorInvalidValue;
-    }
-    Params p;
-    p.offsets = offsets;
-    p.E = s.E;
-    p.f = s.f;
-    p.g1.K = s.d;
-    p.g1.n_out = s.f;
-    p.g1.n_tiles = (int)n_tiles1;
-    p.g1.transpose_epi = s.d <= kTransposeMaxK;
-    p.g1.out = static_cast<__nv_bfloat16 *>(h_perm);
-    p.g2.K = s.f;
-    p.g2.n_out = s.d;
-    p.g2.n_tiles = (int)n_tiles2;
-    p.g2.transpose_epi = s.f <= kTransposeMaxK;
-    p.g2.out = static_cast<__nv_bfloat16 *>(y_perm);
-    p.ds = ds;
-    // G1 tiles only, then G2 tiles only (the second launch reads h_perm)
-    Params p1 = p, p2 = p;
-    p1.g2.n_tiles = 0;
-    p2.g1.n_tiles = 0;
-    const unsigned grid1 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles1);
-    const unsigned grid2 = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles2);
-    cudaError_t err = launch<CTAS>(grid1, mx, mwgu, mh, mwd, p1, st);
-    if (err != cudaSuccess) return err;
-    return launch<CTAS>(grid2, mx, mwgu, mh, mwd, p2, st);
+    Params p = both;
+    p.experts = experts;
+    if (phase == 1) p.g2.n_tiles = 0;
+    else p.g1.n_tiles = 0;
+    const int64_t n_tiles = phase == 1 ? both.g1.n_tiles : both.g2.n_tiles;
+    const unsigned grid = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles);
+    return launch<CTAS>(grid, mx, mwgu, mh, mwd, p, st);
 }
 
 }  // namespace tc
+
+int grouped_swiglu_tc_launches(const Shape &s) {
+    return tc::tile_mode(s) == tc::kModeHybrid ? 4 : 2;
+}
 
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
@@ -649,11 +660,41 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
         set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
         return cudaErrorInvalidValue;
     }
-    // Pairs (256-row tiles) when experts average >= 512 rows; else 128-row
-    // tiles, which waste less on ragged segments and small batches.
-    if (use_pairs(s))
-        return run<2>(s, info[dev].pairs, mx, mwgu, mh, mwd, offsets, h_perm, y_perm, ds, st);
-    return run<1>(s, info[dev].sms, mx, mwgu, mh, mwd, offsets, h_perm, y_perm, ds, st);
+    const int64_t n_tiles1 = (s.f + BN / 2 - 1) / (BN / 2), n_tiles2 = (s.d + BN - 1) / BN;
+    if (row_tiles_bound(s, BM) * (n_tiles1 + n_tiles2) >= (int64_t)INT32_MAX) {
+        set_error_message("grouped GEMM tile count exceeds 2^31");
+        return cudaErrorInvalidValue;
+    }
+    Params p;
+    p.offsets = offsets;
+    p.E = s.E;
+    p.f = s.f;
+    p.g1.K = s.d;
+    p.g1.n_out = s.f;
+    p.g1.n_tiles = (int)n_tiles1;
+    p.g1.transpose_epi = s.d <= kTransposeMaxK;
+    p.g1.out = static_cast<__nv_bfloat16 *>(h_perm);
+    p.g2.K = s.f;
+    p.g2.n_out = s.d;
+    p.g2.n_tiles = (int)n_tiles2;
+    p.g2.transpose_epi = s.f <= kTransposeMaxK;
+    p.g2.out = static_cast<__nv_bfloat16 *>(y_perm);
+    p.experts = kAllExperts;
+    p.ds = ds;
+    // G1 launches, then G2 launches (G2 reads h_perm; stream order)
+    const TileMode mode = tile_mode(s);
+    const int pairs = info[dev].pairs, sms = info[dev].sms;
+    for (int phase = 1; phase <= 2; ++phase) {
+        if (mode == kModePairs)
+            err = launch_product<2>(s, pairs, mx, mwgu, mh, mwd, p, phase, kAllExperts, st);
+        else if (mode == kModeSingles)
+            err = launch_product<1>(s, sms, mx, mwgu, mh, mwd, p, phase, kAllExperts, st);
+        else if ((err = launch_product<2>(s, pairs, mx, mwgu, mh, mwd, p, phase, kPairExperts, st)) ==
+                 cudaSuccess)
+            err = launch_product<1>(s, sms, mx, mwgu, mh, mwd, p, phase, kSingleExperts, st);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace moe

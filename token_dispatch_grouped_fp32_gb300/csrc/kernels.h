@@ -62,6 +62,9 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
                             const float *scale = nullptr);
 
 // Grouped SwiGLU experts.  bf16: tcgen05 tensor-core path; fp32: SIMT path.
+// Kernel launches of one launch_grouped_swiglu_tc call (2, or 4 when the
+// experts are split between CTA-pair and single-CTA tiles).
+int grouped_swiglu_tc_launches(const Shape &s);
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
                                      const DevStatus &ds, cudaStream_t st);

@@ -257,7 +257,8 @@ int moe_forward_kernel_launches(const moe_config_t *cfg) {
     // the same choices as run_route: tensor cores (weight split, logits, top-k),
     // CUDA cores selecting in the logits launch, or CUDA-core logits + top-k
     const int route = router_tc_eligible(s) ? 3 : router_selects_in_logits(s) ? 1 : 2;
-    return route + 4 /* histogram, scan, scatter, gather */ + 2 /* G1, G2 */ + 1 /* combine */;
+    const int experts = s.bf16 ? grouped_swiglu_tc_launches(s) : 2 /* G1, G2 */;
+    return route + 4 /* histogram, scan, scatter, gather */ + experts + 1 /* combine */;
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) {
