@@ -111,6 +111,14 @@ struct Params {
     int f;              // column offset of the up half in Wgu
     PhaseParams g1, g2;  // a launch runs one of them: the other has n_tiles = 0
     int experts;  // which experts this launch serves: kAllExperts, kPairExperts, kSingleExperts
+    // Ordering against the neighbouring launches (programmatic dependent launch).
+    //  release_late: let the next launch start only after this one's own wait
+    //    for its predecessor, so that by then every earlier kernel has completed.
+    //  overlap_prev: this launch's tiles do not read the previous launch's
+    //    output (its experts are disjoint), so it reads its inputs without
+    //    waiting and waits for the previous launch only before it exits; its
+    //    completion still implies the previous launch's.
+    int release_late, overlap_prev;
     DevStatus ds;
 };
 
@@ -216,7 +224,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmWgu,
                        const __grid_constant__ CUtensorMap tmH,
                        const __grid_constant__ CUtensorMap tmWd, Params p) {
-    pdl_release();  // the wait for the previous kernel follows this CTA's own set-up
+    if (!p.release_late) pdl_release();  // the wait below follows this CTA's own set-up
     using C = Cfg<CTAS>;
     constexpr bool PAIR = C::PAIR;
     constexpr int STAGES = C::STAGES;
@@ -262,8 +270,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) tmem_alloc<CTAS>(base_s + C::OFF_TMEM, TMEM_COLS);
-    pdl_wait();
-    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = p.offsets[e];
+    if (!p.overlap_prev) pdl_wait();
+    if (p.release_late) pdl_release();
+    // through L2: with overlap_prev no grid-wide wait precedes this read
+    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = __ldcg(p.offsets + e);
     __syncthreads();
     if (warp == 2) {  // prefix over experts of their row tiles in this launch
         const int per = (E + 31) / 32;
@@ -540,6 +550,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     if constexpr (PAIR) cluster_sync();  // no CTA leaves while its peer may still signal it
     tc_fence_after();
     if (warp == 1) tmem_dealloc<CTAS>(tmem_base, TMEM_COLS);
+    if (p.overlap_prev) pdl_wait();  // this grid completes only after the previous one
 }
 
 // ------------------------------ host side ----------------------------------
@@ -621,6 +632,20 @@ cudaError_t launch_product(const Shape &s, int units, const CUtensorMap &mx,
     return launch<CTAS>(grid, mx, mwgu, mh, mwd, p, st);
 }
 
+// The hybrid sequence: pairs then single CTAs, per product.  The single-CTA
+// launch serves other experts than the pair launch before it, so it overlaps
+// that launch's last partial round (see Params::overlap_prev); the pair
+// launch releases it only once every earlier kernel has completed.
+template <int CTAS>
+cudaError_t launch_product_ordered(const Shape &s, int units, const CUtensorMap &mx,
+                                   const CUtensorMap &mwgu, const CUtensorMap &mh,
+                                   const CUtensorMap &mwd, Params both, int phase, int experts,
+                                   int release_late, int overlap_prev, cudaStream_t st) {
+    both.release_late = release_late;
+    both.overlap_prev = overlap_prev;
+    return launch_product<CTAS>(s, units, mx, mwgu, mh, mwd, both, phase, experts, st);
+}
+
 }  // namespace tc
 
 int grouped_swiglu_tc_launches(const Shape &s) {
@@ -680,6 +705,8 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     p.g2.transpose_epi = s.f <= kTransposeMaxK;
     p.g2.out = static_cast<__nv_bfloat16 *>(y_perm);
     p.experts = kAllExperts;
+    p.release_late = 0;
+    p.overlap_prev = 0;
     p.ds = ds;
     // G1 launches, then G2 launches (G2 reads h_perm; stream order)
     const TileMode mode = tile_mode(s);
@@ -689,9 +716,10 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
             err = launch_product<2>(s, pairs, mx, mwgu, mh, mwd, p, phase, kAllExperts, st);
         else if (mode == kModeSingles)
             err = launch_product<1>(s, sms, mx, mwgu, mh, mwd, p, phase, kAllExperts, st);
-        else if ((err = launch_product<2>(s, pairs, mx, mwgu, mh, mwd, p, phase, kPairExperts, st)) ==
-                 cudaSuccess)
-            err = launch_product<1>(s, sms, mx, mwgu, mh, mwd, p, phase, kSingleExperts, st);
+        else if ((err = launch_product_ordered<2>(s, pairs, mx, mwgu, mh, mwd, p, phase, kPairExperts,
+                                                  1, 0, st)) == cudaSuccess)
+            err = launch_product_ordered<1>(s, sms, mx, mwgu, mh, mwd, p, phase, kSingleExperts, 0, 1,
+                                            st);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
