@@ -6,13 +6,15 @@
 // (experts_forward runs each expert on the rows sent to it), and "Tensor
 // parallelism for inference", section "Packed strategies" (gate_up_proj is
 // [E][d][2f], applied as x @ gate_up_proj and split into gate = first f
-// columns, up = last f columns).  Two launches of one persistent kernel:
+// columns, up = last f columns).  Launches of one persistent kernel compute
 //   G1: h_perm[r] = silu(x_perm[r] @ Wgu[e][:, :f]) * (x_perm[r] @ Wgu[e][:, f:])
 //   G2: y_perm[r] = h_perm[r] @ Wd[e]
 // for every expert e and row r of its segment [offsets[e], offsets[e+1]).
 // The kernel's tile list is every G1 tile, then every G2 tile, and each
 // launch is given the column tiles of one product only (the other's count is
 // zero), so the product is a property of the tile, not of the template.
+// One launch per product when one tile shape serves every expert; two when
+// the experts are split between the shapes (see tile_mode).
 //
 // Tiling.  Two tile shapes share one kernel template (CTAS = 1 or 2).
 //  - CTAS = 2 (a cluster of 2, tcgen05.mma.cta_group::2): the pair owns a
@@ -24,7 +26,8 @@
 //  - CTAS = 1 (tcgen05.mma.cta_group::1): a CTA owns a 128 x 256 tile and
 //    loads 16 KB of A and 32 KB of B per K step (four stages).  Row tiles of
 //    128 waste less on ragged segments, so it serves small per-expert batches
-//    (decode, or ~256 rows per expert), where the weight stream bounds.
+//    (decode), and at ~256 rows per expert the experts that 256-row tiles
+//    would pad more (pair_tiles_pay), where the weight stream bounds.
 // A K step is 64 elements (128 bytes: one swizzle span).  In G1 the 256
 // accumulator columns are 128 gate columns and the 128 matching up columns,
 // so the SwiGLU is applied in the epilogue straight from the two halves of
@@ -33,8 +36,9 @@
 // repacking is needed.
 //
 // Work list.  Row tiles never straddle experts: expert e owns
-// ceil(count_e / tile rows) row tiles and each CTA derives the prefix of
-// those counts from `offsets` on the device (no host synchronisation).
+// ceil(count_e / tile rows) row tiles (none in a launch that serves other
+// experts) and each CTA derives the prefix of those counts from `offsets` on
+// the device (no host synchronisation).
 // Tiles are ordered expert-major, then column tile, then row tile, so tiles
 // running at the same time share the same weight tile through L2.  The grid
 // is persistent (as many CTAs or pairs as fit at once) and strides over the
