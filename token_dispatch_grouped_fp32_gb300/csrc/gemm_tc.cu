@@ -123,6 +123,9 @@ struct Params {
     //    waiting and waits for the previous launch only before it exits; its
     //    completion still implies the previous launch's.
     int release_late, overlap_prev;
+    // B maps are the 64-column-block views (tensor_map_weight_blocks): one
+    // box carries two 8 KB atoms
+    int b_blocks;
     DevStatus ds;
 };
 
@@ -344,6 +347,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     }
                     tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, tmA, k0, arow, fb);
                     const uint32_t bdst = base_s + C::OFF_B + s * C::B_BYTES;
+                    if (p.b_blocks) {
+                        // two atoms per box (weights viewed by 64-column blocks)
+#pragma unroll
+                        for (int a = 0; a < C::B_ATOMS; a += 2) {
+                            int col = n0 + 64 * a;
+                            if (!PAIR && !ti.down && a >= 2) col = ti.n_blk * (BN / 2) + p.f;
+                            tma_load_4d<CTAS>(bdst + a * B_ATOM_BYTES, tmB, 0, k0, col >> 6, ti.e, fb);
+                        }
+                    } else
 #pragma unroll
                     for (int a = 0; a < C::B_ATOMS; ++a) {
                         int col = n0 + 64 * a;
@@ -683,9 +695,16 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     }
     const int64_t P = s.P();
     CUtensorMap mx, mwgu, mh, mwd;
-    if (!tensor_map_rows(&mx, x_perm, P, s.d, BM) ||
-        !tensor_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) ||
-        !tensor_map_rows(&mh, h_perm, P, s.f, BM) || !tensor_map_weights(&mwd, Wd, s.E, s.f, s.d)) {
+    // whole 64-column blocks in both products (gate, up and down columns):
+    // B boxes of two atoms; else one atom per box
+    const bool blocks = s.f % 64 == 0 && s.d % 64 == 0;
+    const bool maps_ok =
+        blocks ? tensor_map_weight_blocks(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f, 2) &&
+                     tensor_map_weight_blocks(&mwd, Wd, s.E, s.f, s.d, 2)
+               : tensor_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) &&
+                     tensor_map_weights(&mwd, Wd, s.E, s.f, s.d);
+    if (!maps_ok || !tensor_map_rows(&mx, x_perm, P, s.d, BM) ||
+        !tensor_map_rows(&mh, h_perm, P, s.f, BM)) {
         set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
         return cudaErrorInvalidValue;
     }
@@ -711,6 +730,7 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     p.experts = kAllExperts;
     p.release_late = 0;
     p.overlap_prev = 0;
+    p.b_blocks = blocks ? 1 : 0;
     p.ds = ds;
     // G1 launches, then G2 launches (G2 reads h_perm; stream order)
     const TileMode mode = tile_mode(s);

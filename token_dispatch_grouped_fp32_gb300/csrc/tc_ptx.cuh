@@ -91,6 +91,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *tm,
             "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
             : "memory");
 }
+template <int CTAS>
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+    if constexpr (CTAS == 2)
+        asm volatile(
+            "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+            : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -287,6 +303,23 @@ inline bool tensor_map_weights(CUtensorMap *m, const void *ptr, int64_t E, int64
     cuuint32_t box[3] = {64, 64, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr),
+                                dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same weights viewed as E x K x (N/64) x 64 (N a multiple of 64): a box
+// of 64 cols x 64 K-rows x `blocks` column blocks lands as `blocks`
+// consecutive 8 KB atoms, the layout the 3-D box gives one atom at a time.
+// Column blocks past N/64 read zeros.
+inline bool tensor_map_weight_blocks(CUtensorMap *m, const void *ptr, int64_t E, int64_t K,
+                                     int64_t N, uint32_t blocks) {
+    if (N % 64 != 0) return false;
+    cuuint64_t dims[4] = {64, (cuuint64_t)K, (cuuint64_t)(N / 64), (cuuint64_t)E};
+    cuuint64_t strides[3] = {(cuuint64_t)N * 2, 128, (cuuint64_t)K * N * 2};
+    cuuint32_t box[4] = {64, 64, blocks, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    return tensor_map_encoder()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr),
                                 dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
