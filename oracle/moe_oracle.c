@@ -38,8 +38,9 @@
  * forms for two-expert softmax and all-equal logits, a sort-based top-k and a
  * stable argsort for the permutation, the dense SwiGLU MLP for E=1,k=1
  * through library matmuls, the dense soft mixture for k=E without
- * renormalisation, and a hand-worked SwiGLU fixture.  Every function below
- * is covered by at least one of them.
+ * renormalisation, a hand-worked SwiGLU fixture, and one-hot expert rows for
+ * the combine (each output entry is then exactly one routing weight).  Every
+ * function below is covered by at least one of them.
  */
 #include <math.h>
 #include <stdint.h>
@@ -226,6 +227,28 @@ void oracle_expert_ffn_row(int32_t d, int32_t f, const float *xrow,
 }
 
 /*
+ * The same FFN on n independent rows [EP-add: experts_forward runs each
+ * expert on the rows sent to it]: row r goes through expert expert[r] of the
+ * given weight block (Wgu [ne][d][2f], Wd [ne][f][d]; expert[r] indexes that
+ * block).  h is [n][f], y is [n][d].  Each row is exactly
+ * oracle_expert_ffn_row; rows are spread over threads, nothing else changes.
+ */
+void oracle_expert_ffn_rows(int64_t n, int32_t d, int32_t f, const float *x,
+                            const int32_t *expert, const float *Wgu,
+                            const float *Wd, double *h, double *y)
+{
+    int64_t r;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (r = 0; r < n; ++r) {
+        double *gu = (double *)malloc(sizeof(double) * 2 * (size_t)f);
+        int64_t e = expert[r];
+        expert_ffn_row_scaled(d, f, x + r * d, 1.0, Wgu + e * (int64_t)d * 2 * f,
+                              Wd + e * (int64_t)f * d, gu, h + r * f, y + r * d);
+        free(gu);
+    }
+}
+
+/*
  * Layer output of selected tokens [EP-add, EP-disp]: for each listed token t,
  * out[n] = sum over slots j = 0..k-1, in slot order, of
  *   w[t][j] * FFN_{idx[t][j]}(x[t])        (scale_inputs == 0), or
@@ -265,6 +288,34 @@ void oracle_token_outputs(int64_t ntok, const int64_t *tokens, int32_t d,
         free(gu);
         free(h);
         free(y);
+    }
+}
+
+/*
+ * Combine [EP-add: each token's weighted expert output; EP-disp: the expert
+ * results come back and are combined with the routing weights]:
+ *   out[t] = sum over slots j = 0..k-1, in slot order, of
+ *            w[t][j] * y_perm[pos[t*k+j]]
+ * (scale_inputs != 0: the weights were applied to the expert inputs, so the
+ * rows are summed unweighted and w is not read).  y_perm [P][d], pos [P],
+ * w [T][k], out [T][d].
+ */
+void oracle_combine(int64_t T, int32_t k, int32_t d, const double *y_perm,
+                    const int32_t *pos, const double *w, int32_t scale_inputs,
+                    double *out)
+{
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; ++t) {
+        double *o = out + t * d;
+        for (int32_t c = 0; c < d; ++c)
+            o[c] = 0.0;
+        for (int32_t j = 0; j < k; ++j) {
+            const double *yr = y_perm + (int64_t)pos[t * k + j] * d;
+            double wj = scale_inputs ? 1.0 : w[t * k + j];
+            for (int32_t c = 0; c < d; ++c)
+                o[c] += wj * yr[c];
+        }
     }
 }
 
@@ -315,19 +366,7 @@ void oracle_moe_forward(int64_t T, int32_t d, int32_t E, int32_t k, int32_t f,
         free(h);
     }
 
-    int64_t t;
-#pragma omp parallel for schedule(static)
-    for (t = 0; t < T; ++t) {
-        double *o = out + t * d;
-        for (int32_t c = 0; c < d; ++c)
-            o[c] = 0.0;
-        for (int32_t j = 0; j < k; ++j) {
-            const double *yr = y_perm + (int64_t)pos[t * k + j] * d;
-            double wj = scale_inputs ? 1.0 : w[t * k + j];
-            for (int32_t c = 0; c < d; ++c)
-                o[c] += wj * yr[c];
-        }
-    }
+    oracle_combine(T, k, d, y_perm, pos, w, scale_inputs, out);
     free(y_perm);
     free(row_expert);
     free(row_scale);

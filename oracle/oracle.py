@@ -48,11 +48,14 @@ def _bind(lib):
     lib.oracle_topk.argtypes = [i64, i32, i32, i32, vp, vp, vp]
     lib.oracle_dispatch.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp]
     lib.oracle_expert_ffn_row.argtypes = [i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_expert_ffn_rows.argtypes = [i64, i32, i32, vp, vp, vp, vp, vp, vp]
+    lib.oracle_combine.argtypes = [i64, i32, i32, vp, vp, vp, i32, vp]
     lib.oracle_token_outputs.argtypes = [i64, vp, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]
     lib.oracle_moe_forward.argtypes = [i64, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp,
                                        vp, vp, vp, vp, vp, vp, vp, vp]
     for fn in ("oracle_router_logits", "oracle_topk", "oracle_dispatch",
-               "oracle_expert_ffn_row", "oracle_token_outputs", "oracle_moe_forward"):
+               "oracle_expert_ffn_row", "oracle_expert_ffn_rows", "oracle_combine",
+               "oracle_token_outputs", "oracle_moe_forward"):
         getattr(lib, fn).restype = None
     return lib
 
@@ -178,6 +181,35 @@ def expert_ffn_row(xrow, Wgu_e, Wd_e):
     return h, y
 
 
+def expert_ffn_rows(x_rows, expert, Wgu, Wd):
+    """The expert FFN on many rows at once: row r of x_rows [n, d] through
+    expert expert[r] of the weight block Wgu [ne, d, 2f], Wd [ne, f, d].
+    Returns (h [n, f], y [n, d]) in float64, each row exactly expert_ffn_row."""
+    x_rows, Wgu, Wd, expert = _f32(x_rows), _f32(Wgu), _f32(Wd), _i32(expert)
+    n, d = x_rows.shape
+    f = Wd.shape[1]
+    assert expert.shape == (n,) and (n == 0 or (expert.min() >= 0 and expert.max() < Wgu.shape[0]))
+    h = np.empty((n, f), np.float64)
+    y = np.empty((n, d), np.float64)
+    _L().oracle_expert_ffn_rows(n, d, f, _p(x_rows), _p(expert), _p(Wgu), _p(Wd), _p(h), _p(y))
+    return h, y
+
+
+def combine(y_perm, pos, w, k, scale_inputs=False):
+    """Combine [T, d] (float64) of the expert rows y_perm [P, d]: token t sums
+    w[t, j] * y_perm[pos[t*k + j]] over its slots j in order (unweighted with
+    scale_inputs)."""
+    y_perm = np.ascontiguousarray(y_perm, dtype=np.float64)
+    pos = _i32(pos).reshape(-1)
+    P, d = y_perm.shape
+    T = pos.shape[0] // k
+    assert pos.shape[0] == T * k and (P == 0 or (pos.min() >= 0 and pos.max() < P))
+    wd = np.ascontiguousarray(np.zeros((T, k)) if w is None else w, dtype=np.float64)
+    out = np.empty((T, d), np.float64)
+    _L().oracle_combine(T, k, d, _p(y_perm), _p(pos), _p(wd), int(bool(scale_inputs)), _p(out))
+    return out
+
+
 def token_outputs(tokens, x, Wgu, Wd, idx, w, scale_inputs=False):
     """Layer output rows [len(tokens), d] (float64) for the listed tokens.
     scale_inputs: the routing weights scale each expert's input instead of
@@ -231,6 +263,6 @@ def _method(fn):
     return m
 
 
-for _fn in (num_threads, router_logits, topk, dispatch, expert_ffn_row, token_outputs,
-            moe_forward):
+for _fn in (num_threads, router_logits, topk, dispatch, expert_ffn_row, expert_ffn_rows, combine,
+            token_outputs, moe_forward):
     setattr(Oracle, _fn.__name__, _method(_fn))

@@ -29,6 +29,10 @@ CHECKS = [
     ("input_scaled_dense", lambda o: pins.test_input_scaled_equals_dense_no_dispatch(o, 6, 2, True)),
     ("input_scaled_kE", lambda o: pins.test_input_scaled_equals_dense_no_dispatch(o, 6, 6, False)),
     ("input_scaled_one_expert", lambda o: pins.test_input_scaled_single_expert_is_plain_mlp(o)),
+    ("combine_one_hot", lambda o: pins.test_combine_one_hot_rows(o, False)),
+    ("combine_one_hot_scaled", lambda o: pins.test_combine_one_hot_rows(o, True)),
+    ("combine_vs_einsum", lambda o: pins.test_combine_matches_einsum_on_random_rows(o)),
+    ("ffn_rows", lambda o: pins.test_expert_ffn_rows_equal_single_rows(o)),
 ]
 
 if __name__ == "__main__":

@@ -35,6 +35,9 @@ MUTANTS = {
     "input_scale_ignored": ("        row_scale[pos[q]] = scale_inputs ? w[q] : 1.0;",
                             "        row_scale[pos[q]] = 1.0;"),
     "bias_dropped": ("            if (bias)\n                s += (double)bias[e];", "            (void)bias;"),
+    "batched_rows_one_expert": ("        int64_t e = expert[r];", "        int64_t e = expert[0];"),
+    "combine_slot_order_reversed": ("            const double *yr = y_perm + (int64_t)pos[t * k + j] * d;",
+                                    "            const double *yr = y_perm + (int64_t)pos[t * k + (k - 1 - j)] * d;"),
     "router_weight_transposed": ("s += (double)x[t * d + i] * (double)Wr[(int64_t)e * d + i];",
                                  "s += (double)x[t * d + i] * (double)Wr[(int64_t)i * E + e];"),
 }

@@ -238,3 +238,57 @@ def test_input_scaled_single_expert_is_plain_mlp(oracle):
     c = oracle.token_outputs(toks, x, Wgu, Wd, np.zeros((17, 1), np.int32), np.ones((17, 1)),
                              scale_inputs=True)
     np.testing.assert_array_equal(c, a[toks])
+
+
+@pytest.mark.parametrize("scale_inputs", [False, True])
+def test_combine_one_hot_rows(oracle, scale_inputs):
+    """Combine on one-hot expert rows: row r of y_perm is the unit vector of
+    column r, so out[t] holds w[t, j] exactly at column pos[t*k + j] (1 when
+    the weights scaled the inputs) and 0 elsewhere -- no rounding anywhere, so
+    the comparison is exact.  Distinct random weights per slot catch a weight
+    taken from the wrong slot."""
+    T, E, k = 40, 8, 3
+    L = synth.make_logits(T, E, 71).numpy()
+    idx, w = oracle.topk(L, k, True)
+    _, _, pos, _ = oracle.dispatch(idx, E)
+    P = T * k
+    y_perm = np.eye(P)
+    out = oracle.combine(y_perm, pos, w, k, scale_inputs=scale_inputs)
+    expect = np.zeros((T, P))
+    for t in range(T):
+        for j in range(k):
+            expect[t, pos[t * k + j]] = 1.0 if scale_inputs else w[t, j]
+    np.testing.assert_array_equal(out, expect)
+
+
+def test_combine_matches_einsum_on_random_rows(oracle):
+    """Random expert rows: the combine equals a float64 gather-and-weigh with
+    numpy (a library routine), to rounding."""
+    T, E, k, d = 57, 16, 4, 24
+    L = synth.make_logits(T, E, 72).numpy()
+    idx, w = oracle.topk(L, k, False)
+    _, _, pos, _ = oracle.dispatch(idx, E)
+    y_perm = np.random.default_rng(4).normal(size=(T * k, d))
+    out = oracle.combine(y_perm, pos, w, k)
+    ref = np.einsum("tk,tkd->td", w, y_perm[pos.reshape(T, k)])
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-15)
+
+
+def test_expert_ffn_rows_equal_single_rows(oracle):
+    """The batched expert FFN is the single-row FFN on every row (bit-equal),
+    each row through its own expert of the block."""
+    rng = np.random.default_rng(5)
+    ne, d, f, n = 3, 24, 16, 11
+    x = rng.normal(size=(n, d)).astype(np.float32)
+    Wgu = (rng.normal(size=(ne, d, 2 * f)) / np.sqrt(d)).astype(np.float32)
+    Wd = (rng.normal(size=(ne, f, d)) / np.sqrt(f)).astype(np.float32)
+    expert = rng.integers(0, ne, size=n).astype(np.int32)
+    h, y = oracle.expert_ffn_rows(x, expert, Wgu, Wd)
+    for r in range(n):
+        h1, y1 = oracle.expert_ffn_row(x[r], Wgu[expert[r]], Wd[expert[r]])
+        np.testing.assert_array_equal(h[r], h1)
+        np.testing.assert_array_equal(y[r], y1)
+    # and against the library form of the FFN
+    for r in range(n):
+        np.testing.assert_allclose(y[r], _np_expert(x[r], Wgu[expert[r]], Wd[expert[r]]),
+                                   rtol=1e-12, atol=1e-13)
