@@ -92,9 +92,36 @@ const char *moe_last_error_message(void);
  * Bytes of workspace moe_forward needs for `cfg` (0 when T == 0).  The same
  * buffer also satisfies moe_route and moe_dispatch.  The workspace holds the
  * router logits and scratch, routing, dispatch arrays and the permuted
- * activations x_perm, h_perm and y_perm; see moe_forward.
+ * activations x_perm, h_perm and y_perm (see moe_workspace_layout).  The
+ * router's share depends on the current device's SM count (its K splits
+ * fill one wave); with no usable device it is sized for 152 SMs.
  */
 size_t moe_workspace_size(const moe_config_t *cfg);
+
+/*
+ * Where moe_forward keeps its intermediates inside its workspace: byte
+ * offsets from the start of the buffer (each 256-byte aligned).  After a
+ * moe_forward call has completed, these regions hold that call's router
+ * logits, routing, dispatch arrays and permuted activations, so a caller can
+ * read, for instance, the chosen experts and weights of every token.
+ *   logits    float [T][E]   (including logit_bias)
+ *   topk_idx  int32 [T][k],  topk_w float [T][k]
+ *   counts    int32 [E],     offsets int32 [E+1]
+ *   pos       int32 [P],     src_token int32 [P]   (as moe_dispatch defines them)
+ *   x_perm    act [P][d],    h_perm act [P][f],    y_perm act [P][d]
+ *   total     = moe_workspace_size(cfg)
+ * Any other bytes of the workspace are library scratch.  T == 0 gives all
+ * zeros.  Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a config
+ * moe_forward would reject, or a NULL `layout`.  Launches nothing (it only
+ * queries the current device's SM count, as moe_workspace_size does).
+ */
+typedef struct {
+    size_t logits, topk_idx, topk_w, counts, offsets, pos, src_token;
+    size_t x_perm, h_perm, y_perm;
+    size_t total;
+} moe_workspace_layout_t;
+
+moe_status_t moe_workspace_layout(const moe_config_t *cfg, moe_workspace_layout_t *layout);
 
 /* Bytes of workspace moe_dispatch needs for `cfg` (per-block histograms). */
 size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
@@ -180,18 +207,26 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
  * host framework owns all device memory and passes only the layer's inputs
  * and outputs, or a service that must not call cudaMalloc after start-up.
  * The histogram scratch moe_dispatch would take from `ws` lives instead in a
- * fixed 1 MiB array inside the library (262,144 int32 entries, held on every
- * GPU that loads the library until the process exits).  Results are
+ * fixed 1 MiB array inside the library (262,144 int32 entries).  Results are
  * identical to moe_dispatch.  This call allocates nothing and calls no
  * allocating routine.
+ * The array belongs to the library's device code.  With CUDA's lazy module
+ * loading (the default), that code, and with it the array's 1 MiB, may be
+ * loaded onto a device only when the library first uses the device; from
+ * then on the device holds it until the process exits.  A service that must
+ * not commit device memory once it is serving should therefore make one
+ * call (any T > 0) on each device at start-up.
  *
  * Limit: moe_dispatch_workspace_size(cfg) must be <= 1 MiB (E times the
  * number of 2048-pair chunks <= 262,144: any P for E <= 256; P <= 524,288
  * for E = 1024); larger sizes return MOE_ERR_UNSUPPORTED and launch nothing.
  * Set-up: the first call with T > 0 on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current, once; make that
- * first call before any stream capture.  All calls on a device share the
- * array, so calls whose kernels overlap on the GPU race: serialise them.
+ * address (cudaGetSymbolAddress) with that device current, once, and keeps
+ * it; make that first call before any stream capture.  The kept address is
+ * not refreshed, so a device reset (cudaDeviceReset, or a teardown and
+ * re-creation of the primary context) after the first call is not
+ * supported.  All calls on a device share the array, so calls whose kernels
+ * overlap on the GPU race: serialise them.
  * Other arguments, errors and outputs are as for moe_dispatch.
  */
 moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int32_t *topk_idx,
@@ -265,8 +300,15 @@ moe_status_t moe_last_device_error(void *stream);
  * Limit, in nanoseconds, on every bounded device-side wait of later launches
  * from this process (default 2e9 = 2 s; 0 restores the default).  A wait
  * that runs out records MOE_ERR_DEVICE_TIMEOUT and the kernel returns.
+ * Limits below 10 ms are raised to 10 ms (unless the test hook
+ * moe_debug_inject_wait_timeout is on): a CTA pair that gave up within one
+ * pipeline stage could otherwise leave a copy in flight that no barrier of
+ * its pair expects.
  */
 void moe_set_wait_limit_ns(uint64_t ns);
+
+/* The wait limit later launches will use, after the 10 ms floor. */
+uint64_t moe_wait_limit_ns(void);
 
 /*
  * Test hook for the failure path (no counterpart on the pages).  While

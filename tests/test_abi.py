@@ -159,3 +159,49 @@ def test_forward_kernel_launches(moe):
     assert moe.moe_forward_kernel_launches(moe.config(4096, 128, 64, 2, 256, "f32")) == 9
     assert moe.moe_forward_kernel_launches(moe.config(0, 128, 8, 2, 256, "bf16")) == 0
     assert moe.moe_forward_kernel_launches(moe.config(4, 4096, 8, 9, 14336)) == -1
+
+
+def test_wait_limit_has_a_floor_outside_the_test_hook(moe):
+    """A limit below one pipeline stage could let one CTA of a pair abort with
+    a copy in flight that its pair never armed, so limits below 10 ms are
+    raised to 10 ms; only the failure-path test hook may go lower."""
+    try:
+        moe.moe_set_wait_limit_ns(1_000)
+        assert moe.moe_wait_limit_ns() == 10_000_000
+        moe.moe_set_wait_limit_ns(50_000_000)
+        assert moe.moe_wait_limit_ns() == 50_000_000
+        moe.moe_set_wait_limit_ns(1_000_000)
+        moe.moe_debug_inject_wait_timeout(True)
+        assert moe.moe_wait_limit_ns() == 1_000_000
+        moe.moe_debug_inject_wait_timeout(False)
+        assert moe.moe_wait_limit_ns() == 10_000_000
+    finally:
+        moe.moe_debug_inject_wait_timeout(False)
+        moe.moe_set_wait_limit_ns(0)
+    assert moe.moe_wait_limit_ns() == 2_000_000_000
+
+
+@pytest.mark.parametrize("T,d,E,k,f,dtype", [(4096, 4096, 8, 2, 14336, "bf16"),
+                                             (8192, 7168, 256, 8, 2048, "bf16"),
+                                             (64, 128, 8, 2, 256, "f32"), (1, 64, 3, 3, 8, "bf16")])
+def test_workspace_layout(moe, T, d, E, k, f, dtype):
+    """The documented regions of moe_forward's workspace are 256-byte
+    aligned, in order, large enough for their arrays, and inside the total."""
+    cfg = moe.config(T, d, E, k, f, dtype)
+    L = moe.moe_workspace_layout(cfg)
+    es = 2 if dtype == "bf16" else 4
+    P = T * k
+    regions = [("logits", 4 * T * E), ("topk_idx", 4 * P), ("topk_w", 4 * P), ("counts", 4 * E),
+               ("offsets", 4 * (E + 1)), ("pos", 4 * P), ("src_token", 4 * P),
+               ("x_perm", es * P * d), ("h_perm", es * P * f), ("y_perm", es * P * d)]
+    spans = sorted((getattr(L, n), getattr(L, n) + size, n) for n, size in regions)
+    for (a0, a1, n), (b0, _, m) in zip(spans, spans[1:]):
+        assert a1 <= b0, (n, m)  # no overlap
+    for a0, a1, n in spans:
+        assert a0 % 256 == 0, n
+        assert a1 <= L.total, n
+    assert L.total == moe.moe_workspace_size(cfg)
+    z = moe.moe_workspace_layout(moe.config(0, d, E, k, f, dtype))
+    assert z.total == 0 and z.x_perm == 0
+    with pytest.raises(moe.MoEError):
+        moe.moe_workspace_layout(moe.config(4, 64, 8, 9, 8))

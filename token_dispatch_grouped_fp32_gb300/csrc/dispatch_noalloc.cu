@@ -9,8 +9,11 @@
 // moe_dispatch_noalloc keeps that scratch in a fixed-size array in the
 // library's own device memory instead.
 //
-// The array lives in every GPU that loads the library until the process
-// exits.  Every call on a device shares it and it keeps the last call's
+// The array is part of the library's device code, so a device holds it from
+// the time that code is loaded there (with lazy module loading, the first
+// use of the device) until the process exits.  The device address is looked
+// up once per device and kept: a device reset after the first call is not
+// supported.  Every call on a device shares it and it keeps the last call's
 // contents; nothing in it needs to start at zero, because the histogram
 // kernel writes every entry a call reads before the scan reads it.  Calls
 // whose kernels overlap on the GPU (other streams, other threads) race on
@@ -50,10 +53,16 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int3
     if (cfg && cfg->T > 0) {
         int dev = 0;
         cudaError_t e = cudaGetDevice(&dev);
-        if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        if (e != cudaSuccess) {
             moe::set_error_message("moe_dispatch_noalloc: cudaGetDevice: %s",
                                    cudaGetErrorString(e));
             return MOE_ERR_CUDA;
+        }
+        if (dev < 0 || dev >= kMaxDevices) {
+            moe::set_error_message("moe_dispatch_noalloc: device ordinal %d is beyond the %d "
+                                   "devices this library keeps an address for",
+                                   dev, kMaxDevices);
+            return MOE_ERR_UNSUPPORTED;
         }
         std::lock_guard<std::mutex> lock(g_scratch_mutex);
         if (!g_scratch_addr[dev]) {

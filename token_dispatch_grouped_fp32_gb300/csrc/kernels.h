@@ -77,6 +77,13 @@ cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const
 cudaError_t launch_combine(const Shape &s, const void *y_perm, const int32_t *pos, const float *w,
                            void *out, cudaStream_t st);
 
+// Streaming multiprocessors of the current device (queried once per device).
+// Without a usable device (sizing a workspace on a host with no GPU) it is
+// 152, a GB300's count; a launch always plans with the real device's count,
+// and a workspace sized for fewer SMs than the device has is then reported
+// as too small (MOE_ERR_WORKSPACE), never overrun.
+int device_sm_count();
+
 // Last detailed message set by a launcher (thread-local; empty if none).
 void set_error_message(const char *fmt, ...);
 const char *error_message();

@@ -25,8 +25,38 @@ const char *error_message() { return g_msg; }
 // Per-device error word written by kernels (see moe_last_device_error).
 __device__ unsigned g_device_error_word;
 
-static std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+// Floor of the wait limit outside the failure-path test hook: well above the
+// time of one pipeline stage, so an abort never leaves a CTA pair with a copy
+// that one CTA issued and the other never armed.
+constexpr unsigned long long kMinWaitLimitNs = 10000000ull;  // 10 ms
+static std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 static std::atomic<int> g_inject_wait_timeout{0};
+
+unsigned long long effective_wait_limit_ns() {
+    const unsigned long long ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    if (g_inject_wait_timeout.load(std::memory_order_relaxed)) return ns;
+    return ns < kMinWaitLimitNs ? kMinWaitLimitNs : ns;
+}
+
+int device_sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();  // no usable device: clear the error so later calls do not see it
+        return 152;
+    }
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            return 152;
+        }
+        cache[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
 
 namespace {
 
@@ -74,7 +104,7 @@ moe_status_t device_status(DevStatus *out) {
     }
     if (!s.supported) return MOE_ERR_UNSUPPORTED;
     out->err = s.err_word;
-    out->wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+    out->wait_limit_ns = effective_wait_limit_ns();
     out->inject_wait_timeout = g_inject_wait_timeout.load(std::memory_order_relaxed);
     return MOE_OK;
 }
@@ -238,6 +268,32 @@ size_t moe_workspace_size(const moe_config_t *cfg) {
     return ws_layout(s).total;
 }
 
+moe_status_t moe_workspace_layout(const moe_config_t *cfg, moe_workspace_layout_t *layout) {
+    g_msg[0] = 0;
+    Shape s;
+    moe_status_t st = check_cfg(cfg, &s);
+    if (st != MOE_OK) return st;
+    if (!layout) {
+        set_error_message("layout is NULL");
+        return MOE_ERR_INVALID_ARG;
+    }
+    memset(layout, 0, sizeof(*layout));
+    if (s.T == 0) return MOE_OK;
+    const WsLayout L = ws_layout(s);
+    layout->logits = L.logits;
+    layout->topk_idx = L.idx;
+    layout->topk_w = L.w;
+    layout->counts = L.counts;
+    layout->offsets = L.offsets;
+    layout->pos = L.pos;
+    layout->src_token = L.src;
+    layout->x_perm = L.x_perm;
+    layout->h_perm = L.h_perm;
+    layout->y_perm = L.y_perm;
+    layout->total = L.total;
+    return MOE_OK;
+}
+
 size_t moe_route_workspace_size(const moe_config_t *cfg) {
     Shape s;
     if (check_cfg(cfg, &s) != MOE_OK || s.T == 0) return 0;
@@ -262,8 +318,10 @@ int moe_forward_kernel_launches(const moe_config_t *cfg) {
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) {
-    g_wait_limit_ns.store(ns ? ns : 2000000000ull, std::memory_order_relaxed);
+    g_wait_limit_ns.store(ns ? ns : kDefaultWaitLimitNs, std::memory_order_relaxed);
 }
+
+uint64_t moe_wait_limit_ns(void) { return effective_wait_limit_ns(); }
 
 void moe_debug_inject_wait_timeout(int enable) {
     g_inject_wait_timeout.store(enable ? 1 : 0, std::memory_order_relaxed);

@@ -52,8 +52,6 @@ constexpr int R_THREADS = 128;
 constexpr int R_NUM_BARS = 2 * R_MAX_STAGES + 2;  // full, empty, done, drain
 constexpr int R_SMEM_MAX = 210 * 1024;
 constexpr int R_PAIR_STAGE_BUDGET = 200 * 1024;
-constexpr int R_SMS = 152;              // SMs of the device the plan is sized for
-constexpr int R_PAIRS_PER_WAVE = R_SMS / 2;  // CTA pairs resident at once
 constexpr int R_SMEM_PER_SM = 228 * 1024;    // shared memory of one SM (1 KB per CTA reserved)
 
 // Shared-memory plan of one launch (host and device agree on it).
@@ -298,11 +296,12 @@ RouterTcPlan router_tc_plan(const Shape &s) {
     // at least 2 stages (three W' tiles each) or 4 stages (one W' tile each) per CTA
     const int min_stages = m.terms == 3 ? 2 : 4;
     const int64_t max_splits = std::max(1, pl.ks_total / min_stages);
+    const int sms = device_sm_count();  // the plan fills one wave of the current device
     int64_t want;
     if (pl.ctas == 2)  // one wave of pairs: as many K splits as still fit beside the tiles
-        want = std::max<int64_t>(1, R_PAIRS_PER_WAVE / tiles);
+        want = std::max<int64_t>(1, (sms / 2) / tiles);
     else  // as many splits as keep the grid within one wave (CTAs per SM by shared memory)
-        want = std::max<int64_t>(1, R_SMS * std::max(1, R_SMEM_PER_SM / (m.bytes + 1024)) / tiles);
+        want = std::max<int64_t>(1, sms * std::max(1, R_SMEM_PER_SM / (m.bytes + 1024)) / tiles);
     want = std::max<int64_t>(1, std::min<int64_t>(want, max_splits));
     pl.ks_per_split = (int)((pl.ks_total + want - 1) / want);
     pl.splits = (pl.ks_total + pl.ks_per_split - 1) / pl.ks_per_split;

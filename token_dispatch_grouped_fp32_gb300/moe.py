@@ -42,6 +42,12 @@ class moe_config_t(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("scale_inputs", ctypes.c_int32)]
 
 
+class moe_workspace_layout_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets",
+                                               "pos", "src_token", "x_perm", "h_perm", "y_perm",
+                                               "total")]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -66,6 +72,8 @@ def _load():
         "moe_forward_host": ([cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], st),
         "moe_last_device_error": ([vp], st),
         "moe_set_wait_limit_ns": ([ctypes.c_uint64], None),
+        "moe_wait_limit_ns": ([], ctypes.c_uint64),
+        "moe_workspace_layout": ([cfgp, ctypes.POINTER(moe_workspace_layout_t)], st),
         "moe_debug_inject_wait_timeout": ([ctypes.c_int], None),
     }
     for name, (args, res) in sig.items():
@@ -142,6 +150,17 @@ def moe_forward_kernel_launches(cfg: moe_config_t) -> int:
 
 def moe_set_wait_limit_ns(ns: int) -> None:
     _lib.moe_set_wait_limit_ns(int(ns))
+
+
+def moe_wait_limit_ns() -> int:
+    return int(_lib.moe_wait_limit_ns())
+
+
+def moe_workspace_layout(cfg: moe_config_t, raise_on_error=True) -> moe_workspace_layout_t:
+    layout = moe_workspace_layout_t()
+    _check(_lib.moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(layout)),
+           "moe_workspace_layout", raise_on_error)
+    return layout
 
 
 def moe_debug_inject_wait_timeout(enable: bool) -> None:
