@@ -14,6 +14,13 @@ activations in pinned host memory (copies inside the timed region).
 For N > 1 (torchrun) every rank runs its own batch of T tokens on its own GPU
 (no data-path collective: tokens are independent), timing is the max over
 ranks, and `scaling` is "weak".
+
+The line also carries: `roofline` (the grouped GEMM against the bf16 tensor
+peak: the burst figure, or the sustained one when the clocks sampled in the
+timed region show sw_power_cap), `layer_roofline` (the slower of the layer's
+FLOPs at that peak and its minimal HBM bytes at the HBM peak, against the
+step time), a per-kernel breakdown, and `all_workloads`: the other four
+workloads timed the same way (K steps each, L2 flushed between steps).
 """
 from __future__ import annotations
 
@@ -30,6 +37,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s on 1 GB300; GEMM % tensor peak, permute/combine % HBM BW"
+# every bf16 workload of the benchmark; the one named by --workload (default
+# mixtral) is the headline line, the others go in its all_workloads block
+ALL_WORKLOADS = ["mixtral", "gptoss_decode", "gptoss_prefill", "qwen3_zipf", "deepseek"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -241,22 +251,40 @@ def workload_config(w):
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
-def run_ours(args, w):
+def gemm_peak(peaks, clocks):
+    """The bf16 tensor peak the timed GEMM is held to: the sustained
+    (power-capped) figure when sw_power_cap was active under load during the
+    timed region, else the burst figure."""
+    if "sw_power_cap" in (clocks.get("reasons") or []) and peaks.get("bf16_tflops_sustained"):
+        return peaks["bf16_tflops_sustained"], "bf16_tflops_sustained (sw_power_cap active under load)"
+    return peaks["bf16_tflops"], "bf16_tflops (burst: no power cap under load)"
+
+
+def layer_roofline(w, touched, ms, peaks, tflops_peak):
+    """The layer's roofline: the slower of its FLOPs at the tensor peak and
+    its minimal HBM bytes at the HBM peak, against the measured step time.
+    FLOPs: 2*T*d*E (router) + 6*P*d*f (experts).  Bytes: the weights of the
+    experts that received rows, x, out and the router weight."""
+    es = 2 if w.dtype == "bf16" else 4
+    P = w.T * w.k
+    flops = 2.0 * w.T * w.d * w.E + 6.0 * P * w.d * w.f
+    nbytes = touched * 3.0 * w.d * w.f * es + 2.0 * w.T * w.d * es + 4.0 * w.E * w.d
+    t_flops = flops / (tflops_peak * 1e12)
+    t_bytes = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_min = max(t_flops, t_bytes)
+    return {"bound": "tensor" if t_flops >= t_bytes else "hbm", "frac": t_min / (ms * 1e-3),
+            "t_roofline_ms": 1e3 * t_min, "ms": ms, "flops": flops, "bytes": nbytes,
+            "touched_experts": int(touched), "peak_tflops": tflops_peak,
+            "peak_hbm_gbs": peaks["hbm_gbs"]}
+
+
+def measure_workload(moe, w, args, dev, rank, world, flush, with_e2e):
+    """Times moe_forward on workload w (K steps, L2 flushed between steps),
+    then the same launch sequence through the component entry points for the
+    per-kernel breakdown, and (with_e2e) the host-buffer path."""
     import torch
-    import torch.distributed as dist
-    from token_dispatch_grouped_fp32_gb300 import build as _build
     from token_dispatch_grouped_fp32_gb300 import synth
 
-    rank, local_rank, world = dist_env()
-    if world > 1 and not dist.is_initialized():
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local_rank)
-    if rank == 0 or world == 1:
-        _build.build()
-    barrier()
-    from token_dispatch_grouped_fp32_gb300 import moe
-
-    dev = torch.device("cuda", local_rank)
     wr = w.with_(seed=w.seed + 100 * rank) if world > 1 else w
     inp = synth.make_inputs(wr, device=dev)
     x, Wr, Wgu, Wd = inp["x"], inp["Wr"], inp["Wgu"], inp["Wd"]
@@ -266,13 +294,14 @@ def run_ours(args, w):
     cfg = layer.config(T)
     ws = layer.workspace(T)
     out = torch.empty_like(x)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
         moe.moe_forward(cfg, x, Wr, bias, Wgu, Wd, out, ws, stream=stream)
 
-    for _ in range(args.warmup):
+    # warm-up: the layer and the L2 flush both run before the timed region
+    for i in range(args.warmup):
+        flush.fill_(float(-i))
         step()
     torch.cuda.synchronize()
     moe.moe_last_device_error()
@@ -280,7 +309,7 @@ def run_ours(args, w):
     # ---- timed region: K steps of moe_forward, per-step events ----
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
-    with ClockSampler(local_rank) as clocks:
+    with ClockSampler(dev.index) as clocks:
         barrier()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
@@ -295,7 +324,10 @@ def run_ours(args, w):
     step_ms = [a.elapsed_time(b) for a, b in evs]
     moe.moe_last_device_error()
     ms = max_over_ranks(sum(step_ms) / len(step_ms), dev)
-    value = aggregate_throughput(T, world, ms / 1e3)
+    clk = clocks.summary()
+    L = moe.moe_workspace_layout(cfg)
+    counts = ws[L.counts:L.counts + 4 * w.E].view(torch.int32).cpu()
+    touched = int((counts > 0).sum())
 
     # ---- per-kernel breakdown: the same launch sequence through the
     # component entry points, events between the calls ----
@@ -303,7 +335,7 @@ def run_ours(args, w):
     logits = torch.empty(T, w.E, dtype=torch.float32, device=dev)
     idx = torch.empty(T, w.k, dtype=torch.int32, device=dev)
     wt = torch.empty(T, w.k, dtype=torch.float32, device=dev)
-    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    cnt = torch.empty(w.E, dtype=torch.int32, device=dev)
     offsets = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
     pos = torch.empty(P, dtype=torch.int32, device=dev)
     src = torch.empty(P, dtype=torch.int32, device=dev)
@@ -319,7 +351,7 @@ def run_ours(args, w):
         if ev: ev[0].record(stream)
         moe.moe_route(cfg, x, Wr, bias, logits, idx, wt, rws, stream=stream)
         if ev: ev[1].record(stream)
-        moe.moe_dispatch(cfg, idx, wt, x, counts, offsets, pos, src, x_perm, dws, stream=stream)
+        moe.moe_dispatch(cfg, idx, wt, x, cnt, offsets, pos, src, x_perm, dws, stream=stream)
         if ev: ev[2].record(stream)
         moe.moe_grouped_swiglu(cfg, x_perm, offsets, Wgu, Wd, h_perm, y_perm, stream=stream)
         if ev: ev[3].record(stream)
@@ -341,9 +373,11 @@ def run_ours(args, w):
     kms = {n: sum(v) / len(v) for n, v in per.items()}
 
     peaks = measured_peaks()
+    peak, peak_name = gemm_peak(peaks, clk)
     es = 2 if w.dtype == "bf16" else 4
     gemm_flops = 6.0 * P * w.d * w.f
     gemm_tflops = gemm_flops / (kms["grouped_swiglu"] * 1e-3) / 1e12
+    weight_bytes = touched * 3.0 * w.d * w.f * es
     # minimal HBM bytes of the bandwidth kernels: dispatch reads each token row
     # once and writes each permuted row once (+ four int32 arrays of P);
     # combine reads the permuted rows and the (pos, weight) pairs and writes
@@ -358,22 +392,28 @@ def run_ours(args, w):
         "dispatch": {"ms": kms["dispatch"], "GB/s": disp_bytes / kms["dispatch"] / 1e6,
                      "frac_hbm": disp_bytes / kms["dispatch"] / 1e6 / hbm},
         "grouped_swiglu": {"ms": kms["grouped_swiglu"], "TFLOP/s": gemm_tflops,
-                           "frac_tensor": gemm_tflops / peaks["bf16_tflops"]},
+                           "frac_tensor": gemm_tflops / peak,
+                           "frac_of_burst_peak": gemm_tflops / peaks["bf16_tflops"],
+                           "weight_stream_GB/s": weight_bytes / kms["grouped_swiglu"] / 1e6,
+                           "frac_hbm_weight_stream":
+                               weight_bytes / kms["grouped_swiglu"] / 1e6 / hbm},
         "combine": {"ms": kms["combine"], "GB/s": comb_bytes / kms["combine"] / 1e6,
                     "frac_hbm": comb_bytes / kms["combine"] / 1e6 / hbm},
         "sum_ms": sum(kms.values()), "same_output_as_moe_forward": same_as_fused,
     }
-    # The GEMM runs back to back inside a long timed loop (power-capped
-    # clocks, see "clocks"), so its denominator is the sustained bf16 peak;
-    # the burst fraction is reported beside it.
-    peak = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peak,
                 "unit": "TFLOP/s", "frac": gemm_tflops / peak,
                 "frac_of_burst_peak": gemm_tflops / peaks["bf16_tflops"],
                 "traffic": recorded_traffic(w), "kernel": "grouped_gemm_tc_kernel (G1 gate/up "
                 "+ SwiGLU, G2 down) via moe_grouped_swiglu",
                 "algorithmic": f"6*P*d*f = {gemm_flops:.4g} FLOP per call (P=T*k={P})",
-                "peak_source": peaks["source"] + " bf16_tflops_sustained"}
+                "peak_source": f"{peaks['source']} {peak_name}"}
+    res = {"w": w, "ms": ms, "value": aggregate_throughput(T, world, ms / 1e3), "kernels": kernels,
+           "roofline": roofline, "clocks": clk, "t_wall": t_wall,
+           "layer_roofline": layer_roofline(w, touched, ms, peaks, peak),
+           "launches_per_step": moe.moe_forward_kernel_launches(cfg), "inp": inp}
+    if not with_e2e:
+        return res
 
     # ---- e2e: activations in pinned host memory, copies inside the region ----
     # Each step copies its x from pinned host memory, runs the layer and copies
@@ -425,29 +465,86 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     e2e_pipe = max_over_ranks(max(start.elapsed_time(ev) for ev in ends) / args.steps, dev)
     moe.moe_last_device_error()
+    res["e2e"] = {"value": aggregate_throughput(T, world, e2e_pipe / 1e3), "unit": "tokens/s",
+                  "h2d_bytes_per_step": T * w.d * es, "d2h_bytes_per_step": T * w.d * es,
+                  "mode": "moe_forward_host, steps alternating on two streams (copies of one "
+                          "step overlap the other's layer)",
+                  "serial_value": aggregate_throughput(T, world, e2e_serial / 1e3)}
+    return res
+
+
+def workload_summary(r):
+    """The per-workload entry of the all_workloads block."""
+    k = r["kernels"]
+    return {"config": workload_config(r["w"]), "value": r["value"], "unit": "tokens/s",
+            "ms_per_step": r["ms"], "layer_roofline": r["layer_roofline"],
+            "gemm": {"ms": k["grouped_swiglu"]["ms"], "TFLOP/s": k["grouped_swiglu"]["TFLOP/s"],
+                     "frac_tensor": k["grouped_swiglu"]["frac_tensor"],
+                     "frac_of_burst_peak": k["grouped_swiglu"]["frac_of_burst_peak"],
+                     "frac_hbm_weight_stream": k["grouped_swiglu"]["frac_hbm_weight_stream"],
+                     "peak_source": r["roofline"]["peak_source"]},
+            "route_ms": k["route"]["ms"],
+            "dispatch": {"ms": k["dispatch"]["ms"], "frac_hbm": k["dispatch"]["frac_hbm"]},
+            "combine": {"ms": k["combine"]["ms"], "frac_hbm": k["combine"]["frac_hbm"]},
+            "same_output_as_moe_forward": k["same_output_as_moe_forward"],
+            "gpu_launches_per_step": r["launches_per_step"], "clocks": r["clocks"]}
+
+
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+    from token_dispatch_grouped_fp32_gb300 import build as _build
+    from token_dispatch_grouped_fp32_gb300 import synth
+
+    rank, local_rank, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    if rank == 0 or world == 1:
+        _build.build()
+    barrier()
+    from token_dispatch_grouped_fp32_gb300 import moe
+
+    dev = torch.device("cuda", local_rank)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    r = measure_workload(moe, w, args, dev, rank, world, flush, with_e2e=True)
 
     line = None
     if rank == 0:
         cpu = None
         if world == 1 and not args.no_cpu_baseline:
-            tps, n, secs, thr = oracle_sample_tokens_per_s(inp, w, args.cpu_budget_s, T)
+            tps, n, secs, thr = oracle_sample_tokens_per_s(r["inp"], w, args.cpu_budget_s, w.T)
             cpu = {"value": tps, "unit": "tokens/s", "cores": thr, "kind": "oracle",
                    "sample": f"first {n} tokens of the workload, whole layer "
                              f"(route, dispatch, experts, combine), {secs:.1f} s"}
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "metric": METRIC, "value": r["value"], "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic", "config": workload_config(w),
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu,
-            "e2e": {"value": aggregate_throughput(T, world, e2e_pipe / 1e3), "unit": "tokens/s",
-                    "h2d_bytes_per_step": T * w.d * es, "d2h_bytes_per_step": T * w.d * es,
-                    "mode": "moe_forward_host, steps alternating on two streams (copies of one "
-                            "step overlap the other's layer)",
-                    "serial_value": aggregate_throughput(T, world, e2e_serial / 1e3)},
-            "gpu_launches": moe.moe_forward_kernel_launches(cfg) * args.steps,
-            "clocks": clocks.summary(), "wall_s_timed_region": t_wall,
+            "roofline": r["roofline"], "layer_roofline": r["layer_roofline"],
+            "kernels": r["kernels"], "cpu_baseline": cpu, "e2e": r["e2e"],
+            "gpu_launches": r["launches_per_step"] * args.steps,
+            "clocks": r["clocks"], "wall_s_timed_region": r["t_wall"],
         }
+    del r
+    torch.cuda.empty_cache()
+
+    # the other workloads, each timed the same way (no e2e, no CPU baseline):
+    # parity-test configurations that the headline line does not cover
+    if not args.no_all_workloads and args.tokens is None:
+        extra = {}
+        for name in ALL_WORKLOADS:
+            if name == w.name:
+                continue
+            rr = measure_workload(moe, synth.WORKLOADS[name], args, dev, rank, world, flush,
+                                  with_e2e=False)
+            extra[name] = workload_summary(rr)
+            del rr
+            torch.cuda.empty_cache()
+        if line is not None:
+            line["all_workloads"] = extra
+    if line is not None:
         print(json.dumps(line), flush=True)
     barrier()
     if world > 1 and dist.is_initialized():
@@ -482,6 +579,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None, help="override T")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-workloads", action="store_true",
+                    help="time only --workload (no all_workloads block)")
     ap.add_argument("--ref-step-s", type=float, default=None,
                     help="host seconds per reference step (default: 120 s / steps, within 0.25-4 s)")
     ap.add_argument("--ref-warmup", action="store_true",
