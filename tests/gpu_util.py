@@ -35,9 +35,9 @@ def fp32_tolerance(ref: np.ndarray, *lengths: int) -> float:
     random sign carries an error of about u * sqrt(n) relative to the scale of
     its result (u = 2^-24); dot products in series (lengths d for gate and up,
     then f for the down projection) add their terms.  The factor 8 is a safety
-    margin.  For the tiny workload (d = 128, f = 256) this is about 1.3e-5 of
-    max|ref|: roughly 10x the errors the fp32 path shows, and 150x below an
-    error of bf16 rounding size (2^-9 relative), which it is there to catch.
+    margin.  For the tiny workload (d = 128, f = 256) this is about 1.8e-5 of
+    max|ref|: roughly 10x the errors the fp32 path shows, and 200x below an
+    error of bf16 rounding size (2^-8 relative), which it is there to catch.
     """
     u = 2.0 ** -24
     scale = float(np.max(np.abs(ref))) if ref.size else 0.0
