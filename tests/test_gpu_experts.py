@@ -42,6 +42,8 @@ EXPERT_CASES = [
     # it less (256-row pairs for 129..256 rows, 128-row single CTAs for 300)
     ([200, 256, 129, 250], 128, 256),   # every expert on pairs: the single-CTA launch is empty
     ([300, 129, 64, 256, 1], 192, 136), # both launches busy
+    # segment ends on both sides of every tile boundary, in both launches
+    ([128, 129, 256, 257, 384, 385, 0, 1, 511, 512, 640], 136, 200),
 ]
 
 
