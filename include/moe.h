@@ -123,12 +123,13 @@ typedef struct {
 
 moe_status_t moe_workspace_layout(const moe_config_t *cfg, moe_workspace_layout_t *layout);
 
-/* Bytes of workspace moe_dispatch needs for `cfg` (per-block histograms). */
+/* Bytes of workspace moe_dispatch needs for `cfg`: the per-chunk expert
+ * count matrix (E x chunks int32) and a 16-byte ticket counter. */
 size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
 
 /*
  * Number of kernel launches one moe_forward call makes for `cfg`: the router
- * (1 to 3 launches, by path), the dispatch (4), the two grouped GEMMs (2, or
+ * (1 to 3 launches, by path), the dispatch (2), the two grouped GEMMs (2, or
  * 4 when bf16 experts average 64 to 511 rows each and are split between two
  * tile shapes) and the combine (1).  0 when T == 0; -1 for an invalid
  * configuration.  Makes no CUDA call.
@@ -193,6 +194,10 @@ moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits,
  * sets MOE_ERR_BAD_ROUTING in the device error word and that pair is dropped.
  * topk_w [T][k] fp32: read only when cfg->scale_inputs (may be NULL otherwise).
  * ws: at least moe_dispatch_workspace_size(cfg) bytes, 256-byte aligned.
+ * Two launches: a rank kernel (per-chunk counts, stable ranks, and, in its
+ * last block, the scan that yields counts and offsets) and a kernel that
+ * places every pair's row and copies it.  The rank kernel's ticket counter
+ * in ws is cleared first with a 4-byte cudaMemsetAsync on `stream`.
  */
 moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
                           const float *topk_w, const void *x, int32_t *counts,
@@ -206,8 +211,8 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
  * For callers that cannot allocate device memory for scratch: a plugin whose
  * host framework owns all device memory and passes only the layer's inputs
  * and outputs, or a service that must not call cudaMalloc after start-up.
- * The histogram scratch moe_dispatch would take from `ws` lives instead in a
- * fixed 1 MiB array inside the library (262,144 int32 entries).  Results are
+ * The scratch moe_dispatch would take from `ws` (its count matrix and ticket
+ * counter) lives instead in a fixed 1 MiB array inside the library.  Results are
  * identical to moe_dispatch.  This call allocates nothing and calls no
  * allocating routine.
  * The array belongs to the library's device code.  With CUDA's lazy module
@@ -218,7 +223,7 @@ moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
  * call (any T > 0) on each device at start-up.
  *
  * Limit: moe_dispatch_workspace_size(cfg) must be <= 1 MiB (E times the
- * number of 2048-pair chunks <= 262,144: any P for E <= 256; P <= 524,288
+ * number of 2048-pair chunks <= 262,140: any P for E <= 256; P <= 522,240
  * for E = 1024); larger sizes return MOE_ERR_UNSUPPORTED and launch nothing.
  * Set-up: the first call with T > 0 on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current, once, and keeps

@@ -49,10 +49,11 @@ def test_workspace_sizes(moe):
     router = 3 * 8 * 4096 * 2 + 32 * 4096 * 8 * 4
     assert perm <= ws <= perm + 4096 * 8 * 4 + 10 * P * 4 + router + 64 * 1024
     assert moe.moe_workspace_size(moe.config(0, 4096, 8, 2, 14336)) == 0
-    # P = 8192 pairs in chunks of 256 (the smallest chunk that keeps <= 256 chunks)
-    assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * (P // 256)
+    # P = 8192 pairs in chunks of 256 (the smallest chunk that keeps <= 256 chunks):
+    # the [E][chunks] count matrix, then the rank kernel's ticket (16 bytes)
+    assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * (P // 256) + 16
     big = moe.config(70000, 8, 1024, 8, 8)  # 560,000 pairs: chunks of 2048
-    assert moe.moe_dispatch_workspace_size(big) == 4 * 1024 * ((560000 + 2047) // 2048)
+    assert moe.moe_dispatch_workspace_size(big) == 4 * 1024 * ((560000 + 2047) // 2048) + 16
     # invalid config -> 0
     assert moe.moe_workspace_size(moe.config(4, 4096, 8, 9, 14336)) == 0
 
@@ -148,15 +149,15 @@ def test_input_scaling_needs_weights_at_dispatch_only(moe):
 def test_forward_kernel_launches(moe):
     """The bench's gpu_launches claim comes from the library's own launch plan."""
     # Mixtral-shaped, bf16, E = 8, T = 4096: tensor-core router (weight split,
-    # logits, top-k) + dispatch (4) + G1, G2 + combine
-    assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 10
+    # logits, top-k) + dispatch (rank, place rows) + G1, G2 + combine
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 8
     # about 256 rows per expert: G1 and G2 each as a CTA-pair launch and a
     # single-CTA launch, the experts split between them
-    assert moe.moe_forward_kernel_launches(moe.config(8192, 2880, 128, 4, 2880, "bf16")) == 12
+    assert moe.moe_forward_kernel_launches(moe.config(8192, 2880, 128, 4, 2880, "bf16")) == 10
     # small batch, E <= 32: logits and selection in one CUDA-core launch
-    assert moe.moe_forward_kernel_launches(moe.config(64, 128, 8, 2, 256, "f32")) == 8
+    assert moe.moe_forward_kernel_launches(moe.config(64, 128, 8, 2, 256, "f32")) == 6
     # fp32 activations, E > 32: CUDA-core logits, then the top-k kernel
-    assert moe.moe_forward_kernel_launches(moe.config(4096, 128, 64, 2, 256, "f32")) == 9
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 128, 64, 2, 256, "f32")) == 7
     assert moe.moe_forward_kernel_launches(moe.config(0, 128, 8, 2, 256, "bf16")) == 0
     assert moe.moe_forward_kernel_launches(moe.config(4, 4096, 8, 9, 14336)) == -1
 

@@ -1,91 +1,84 @@
 // dispatch.cu -- token dispatch on one device: per-expert histogram, exclusive
-// scan, stable scatter into expert-contiguous order, and the row gather.
+// scan, stable scatter into expert-contiguous order, and the row gather, in
+// two launches.
 //
 // Transformers docs "Expert parallelism", section "Token dispatch": every
 // (token, expert) pair is sent to its expert and the experts run on the rows
 // they receive.  On one GPU "sending" is a permutation: pair (t, j) gets row
 // pos[t*k+j] of its expert's segment, segments laid out in expert order.
 //
-// Stability: pairs are cut into chunks of consecutive pair ids; chunk b's
-// rows for expert e start at the exclusive scan of the expert-major
-// [E][chunks] count matrix, and inside a chunk every warp ranks its pairs
-// with __match_any_sync in pair order.  So rows of one expert are in
-// ascending pair id, hence ascending token id, with no atomics deciding order.
+// Launch 1 (rank_kernel), one block per chunk of consecutive pair ids: the
+// block counts its chunk's pairs per expert, writes that column of the
+// expert-major [E][chunks] count matrix, and gives every pair its rank among
+// the chunk's pairs of the same expert (warps rank their pairs with
+// __match_any_sync in pair order, after the counts of the warps before
+// them).  The last block to finish (a ticket counter) scans the matrix into
+// the first row of every (expert, chunk), which also yields counts and
+// offsets, and resets the ticket for the next call.
+// Launch 2 (place_rows_kernel), a block per group of consecutive pairs: row =
+// first row of the pair's (expert, chunk) + its rank; writes pos, src_token
+// and copies the token's row into x_perm.
+// Stability: rows of one expert are in ascending pair id, hence ascending
+// token id, and no atomic decides any order.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace moe {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;      // place_rows_kernel
 constexpr int kWarps = kThreads / 32;
+constexpr int kRankThreads = 1024;  // rank_kernel
+constexpr int kRankWarps = kRankThreads / 32;
+// The count matrix is staged in shared memory for the scan when it has at
+// most this many entries (else the scan reads it through L2).
+constexpr int kScanStageMax = 16 * 1024;
+// rank_kernel packs a pair's expert id and its rank in its chunk into one
+// int: (e << kRankBits) | rank.  E <= 1024 needs 10 bits; a chunk holds at
+// most 2^21 pairs (P < 2^31 in at most 1024 chunks), so its ranks fit 21.
+constexpr int kRankBits = 21;
+constexpr int kRankMask = (1 << kRankBits) - 1;
 
-// counts of chunk b, stored expert-major: hist[e * NB + b]
-__global__ void __launch_bounds__(kThreads)
-chunk_histogram_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB,
-                       int32_t *__restrict__ hist, DevStatus ds) {
-    pdl_entry();
-    extern __shared__ int sh_count[];
-    for (int e = threadIdx.x; e < E; e += kThreads) sh_count[e] = 0;
-    __syncthreads();
-    const int64_t q0 = (int64_t)blockIdx.x * chunk;
-    const int64_t q1 = min(q0 + chunk, P);
-#pragma unroll 8  // independent iterations: several index loads in flight
-    for (int64_t q = q0 + threadIdx.x; q < q1; q += kThreads) {
-        int e = idx[q];
-        if ((unsigned)e < (unsigned)E)
-            atomicAdd(&sh_count[e], 1);
-        else
-            raise_error(ds, kErrBadRouting);
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) hist[(int64_t)e * NB + blockIdx.x] = sh_count[e];
-}
-
-// Single block: exclusive scan of hist[0 .. E*NB) in place (the base row of
-// every (expert, chunk)), then counts[e] and offsets[0..E].  STAGED: the
-// matrix (at most kScanStageMax ints) is first copied to shared memory with
-// coalesced loads, scanned there and copied back, so each thread's serial
-// walk over its segment reads shared memory instead of waiting on one global
-// load after another.
-constexpr int kScanThreads = 1024;
-constexpr int kScanStageMax = 12 * 1024 - 64;  // ints: with the static arrays, under 48 KB
-template <bool STAGED>
-__global__ void __launch_bounds__(kScanThreads)
-scan_kernel(int32_t *__restrict__ hist_g, int E, int NB, int32_t *__restrict__ counts,
-            int32_t *__restrict__ offsets) {
-    pdl_entry();
-    __shared__ int warp_tot[kScanThreads / 32];
+// Exclusive scan, in place, of the expert-major count matrix hist[0 .. E*NB)
+// by one block of kRankThreads: afterwards hist[e*NB + b] is the first row
+// of expert e's pairs in chunk b, counts[e] and offsets[0..E] follow.  The
+// matrix was written by other blocks of the grid, so it is read through L2;
+// `stage` (shared memory for kScanStageMax ints, or nullptr) holds a copy
+// while it is scanned, so the per-thread walks read shared memory.
+__device__ void scan_count_matrix(int32_t *__restrict__ hist_g, int E, int NB,
+                                  int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                                  int *stage) {
+    __shared__ int warp_tot[kRankWarps];
     __shared__ int total_s;
-    extern __shared__ int sh_hist[];
     const int n = E * NB;
     int32_t *hist = hist_g;
-    if (STAGED) {
-        for (int i = threadIdx.x; i < n; i += kScanThreads) sh_hist[i] = hist_g[i];
+    if (stage != nullptr) {
+        for (int i = threadIdx.x; i < n; i += kRankThreads) stage[i] = __ldcg(hist_g + i);
         __syncthreads();
-        hist = sh_hist;
+        hist = stage;
     }
-    const int seg = (n + kScanThreads - 1) / kScanThreads;
+    const int seg = (n + kRankThreads - 1) / kRankThreads;
     const int beg = min(n, (int)threadIdx.x * seg);
     const int end = min(n, beg + seg);
     int local = 0;
-    for (int i = beg; i < end; ++i) local += hist[i];
-    // block exclusive scan of `local`
+    for (int i = beg; i < end; ++i) local += stage != nullptr ? hist[i] : __ldcg(hist + i);
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     int incl = local;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        int v = __shfl_up_sync(0xffffffffu, incl, off);
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
         if (lane >= off) incl += v;
     }
     if (lane == 31) warp_tot[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        int v = warp_tot[lane];
+        const int v = warp_tot[lane];  // kRankWarps == 32
         int inc = v;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            int u = __shfl_up_sync(0xffffffffu, inc, off);
+            const int u = __shfl_up_sync(0xffffffffu, inc, off);
             if (lane >= off) inc += u;
         }
         warp_tot[lane] = inc - v;  // exclusive warp base
@@ -94,50 +87,63 @@ scan_kernel(int32_t *__restrict__ hist_g, int E, int NB, int32_t *__restrict__ c
     __syncthreads();
     int run = warp_tot[wid] + incl - local;
     for (int i = beg; i < end; ++i) {
-        int c = hist[i];
+        const int c = stage != nullptr ? hist[i] : __ldcg(hist + i);
         hist[i] = run;
         run += c;
     }
-    __syncthreads();
-    if (STAGED)
-        for (int i = threadIdx.x; i < n; i += kScanThreads) hist_g[i] = sh_hist[i];
+    __syncthreads();  // the block's writes above are visible to the block
+    if (stage != nullptr)
+        for (int i = threadIdx.x; i < n; i += kRankThreads) hist_g[i] = stage[i];
     const int total = total_s;
-    for (int e = threadIdx.x; e < E; e += kScanThreads) {
-        int b0 = hist[e * NB];
-        int b1 = (e + 1 < E) ? hist[(e + 1) * NB] : total;
+    for (int e = threadIdx.x; e < E; e += kRankThreads) {
+        const int b0 = hist[e * NB];
+        const int b1 = (e + 1 < E) ? hist[(e + 1) * NB] : total;
         offsets[e] = b0;
         counts[e] = b1 - b0;
     }
     if (threadIdx.x == 0) offsets[E] = total;
 }
 
-// Stable scatter: warp w of block b ranks pairs [q0 + w*sub, q0 + (w+1)*sub).
-__global__ void __launch_bounds__(kThreads)
-scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chunk, int NB,
-               const int32_t *__restrict__ base, int32_t *__restrict__ pos,
-               int32_t *__restrict__ src_token) {
+// Launch 1: chunk b = pairs [b*chunk, (b+1)*chunk); warp w of the block ranks
+// the sub-range [q0 + w*sub, q0 + (w+1)*sub).  Writes hist[e*NB + b] (the
+// chunk's count of expert e) and packed[q] = (e << kRankBits) | (the pair's
+// rank among the chunk's pairs of expert e), or -1 for an expert id outside
+// [0, E), which is reported and dropped.  The ticket must be 0 when the
+// launch starts; the last block leaves it 0.  Dynamic shared memory:
+// max(kRankWarps * E, staged count matrix) ints.
+__global__ void __launch_bounds__(kRankThreads)
+rank_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB, int staged,
+            int32_t *__restrict__ hist, int32_t *__restrict__ packed,
+            int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+            unsigned *__restrict__ ticket, DevStatus ds) {
     pdl_entry();
-    extern __shared__ int sh_warp[];  // [kWarps][E]: per-warp counts, then running row
+    extern __shared__ int sh_warp[];  // [kRankWarps][E]: per-warp counts, then first ranks
+    __shared__ int s_last;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kWarps * E; i += kThreads) sh_warp[i] = 0;
+    for (int i = threadIdx.x; i < kRankWarps * E; i += kRankThreads) sh_warp[i] = 0;
     __syncthreads();
-    const int sub = chunk / kWarps;  // multiple of 32
-    const int64_t w0 = (int64_t)blockIdx.x * chunk + (int64_t)wid * sub;
-    const int64_t w1 = min(w0 + sub, P);
+    const int sub = (chunk + kRankWarps - 1) / kRankWarps;
+    const int64_t cend = min((int64_t)(blockIdx.x + 1) * chunk, P);
+    const int64_t w0 = min((int64_t)blockIdx.x * chunk + (int64_t)wid * sub, cend);
+    const int64_t w1 = min(w0 + sub, cend);
     int *mine = sh_warp + wid * E;
-#pragma unroll 8  // independent iterations: several index loads in flight
+#pragma unroll 4  // independent iterations: several index loads in flight
     for (int64_t q = w0 + lane; q < w1; q += 32) {
-        int e = idx[q];
-        if ((unsigned)e < (unsigned)E) atomicAdd(&mine[e], 1);
+        const int e = idx[q];
+        if ((unsigned)e < (unsigned)E)
+            atomicAdd(&mine[e], 1);
+        else
+            raise_error(ds, kErrBadRouting);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) {
-        int run = base[(int64_t)e * NB + blockIdx.x];
-        for (int w = 0; w < kWarps; ++w) {
-            int c = sh_warp[w * E + e];
+    for (int e = threadIdx.x; e < E; e += kRankThreads) {
+        int run = 0;
+        for (int w = 0; w < kRankWarps; ++w) {
+            const int c = sh_warp[w * E + e];
             sh_warp[w * E + e] = run;
             run += c;
         }
+        hist[(int64_t)e * NB + blockIdx.x] = run;
     }
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -149,71 +155,87 @@ scatter_kernel(const int32_t *__restrict__ idx, int64_t P, int k, int E, int chu
         if (q < w1 && (unsigned)e >= (unsigned)E) e = -1;
         e_next = (q + 32 < w1) ? idx[q + 32] : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(peers & lt_mask);
-        const int row0 = (e >= 0) ? mine[e] : 0;
+        const int before = __popc(peers & lt_mask);
+        const int r0 = (e >= 0) ? mine[e] : 0;
         __syncwarp();
         if (q < w1) {
-            if (e >= 0) {
-                const int row = row0 + rank;
-                pos[q] = row;
-                src_token[row] = (int32_t)(q / k);
-                if (lane == 31 - __clz(peers)) mine[e] = row0 + __popc(peers);
-            } else {
-                pos[q] = -1;  // dropped pair (expert id out of range)
-            }
+            packed[q] = (e >= 0) ? ((e << kRankBits) | (r0 + before)) : -1;
+            if (e >= 0 && lane == 31 - __clz(peers)) mine[e] = r0 + __popc(peers);
         }
         __syncwarp();
     }
+    // The last block to get here scans the count matrix.  Every thread makes
+    // its count-matrix writes visible device-wide before the block takes its
+    // ticket; the last block fences again before reading the others'.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(ticket, 1u) == (unsigned)NB - 1u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    scan_count_matrix(hist, E, NB, counts, offsets, staged ? sh_warp : nullptr);
+    if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call (stream order)
 }
 
-// Row gather x_perm[pos[q]] = x[q / k]: one warp per pair, 16-byte vectors.
+// Launch 2: block g places the G pairs [g*G, (g+1)*G) (G divides the chunk,
+// G <= kThreads).  First one thread per pair turns its packed (expert, rank)
+// into its row -- the first row of its (expert, chunk) plus its rank --
+// writes pos[q] and src_token[row]; then the warps copy the token rows into
+// x_perm, one row at a time (16-byte vectors; with SCALE, each element times
+// the pair's weight, formed in fp32 and rounded once).
+template <typename TA, bool SCALE>
 __global__ void __launch_bounds__(kThreads)
-gather_rows_kernel(const uint8_t *__restrict__ x, const int32_t *__restrict__ pos, int64_t P,
-                   int k, int row_vecs, uint8_t *__restrict__ x_perm) {
-    pdl_entry();
-    const int lane = threadIdx.x & 31;
-    const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (q >= P) return;
-    const int row = pos[q];
-    if (row < 0) return;
-    const int64_t t = q / k;
-    const uint4 *src = reinterpret_cast<const uint4 *>(x) + t * row_vecs;
-    uint4 *dst = reinterpret_cast<uint4 *>(x_perm) + (int64_t)row * row_vecs;
-    int i = lane;
-    for (; i + 96 < row_vecs; i += 128) {
-        uint4 a = ldg16(src + i), b = ldg16(src + i + 32), c = ldg16(src + i + 64),
-              d = ldg16(src + i + 96);
-        stg16(dst + i, a);
-        stg16(dst + i + 32, b);
-        stg16(dst + i + 64, c);
-        stg16(dst + i + 96, d);
-    }
-    for (; i < row_vecs; i += 32) stg16(dst + i, ldg16(src + i));
-}
-
-// Scaled row gather x_perm[pos[q]] = scale[q] * x[q / k], the product formed
-// in fp32 and rounded once to the activation dtype.
-template <typename TA>
-__global__ void __launch_bounds__(kThreads)
-gather_rows_scaled_kernel(const TA *__restrict__ x, const int32_t *__restrict__ pos,
-                          const float *__restrict__ scale, int64_t P, int k, int d,
-                          TA *__restrict__ x_perm) {
+place_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist,
+                  const float *__restrict__ scale, int64_t P, int k, int d, int chunk, int NB,
+                  int G, int32_t *__restrict__ pos, int32_t *__restrict__ src_token,
+                  TA *__restrict__ x_perm) {
     pdl_entry();
     constexpr int EPV = 16 / sizeof(TA);
+    __shared__ int s_row[kThreads];
+    const int64_t p0 = (int64_t)blockIdx.x * G;
+    const int n = (int)min((int64_t)G, P - p0);
+    if ((int)threadIdx.x < n) {
+        const int64_t q = p0 + threadIdx.x;
+        const int v = pos[q];  // packed by launch 1
+        int row = -1;          // dropped pair: pos stays -1
+        if (v >= 0) {
+            row = hist[(int64_t)(v >> kRankBits) * NB + (int)(q / chunk)] + (v & kRankMask);
+            pos[q] = row;
+            src_token[row] = (int32_t)(q / k);
+        }
+        s_row[threadIdx.x] = row;
+    }
+    __syncthreads();
+    if (x_perm == nullptr) return;
     const int lane = threadIdx.x & 31;
-    const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (q >= P) return;
-    const int row = pos[q];
-    if (row < 0) return;
-    const float wq = scale[q];
-    const TA *src = x + (q / k) * d;
-    TA *dst = x_perm + (int64_t)row * d;
-    for (int v = lane; v < d / EPV; v += 32) {
-        float f[EPV];
-        unpack16(ldg16(src + (int64_t)v * EPV), f, static_cast<const TA *>(nullptr));
+    const int nvec = d / EPV;
+    for (int i = threadIdx.x >> 5; i < n; i += kWarps) {
+        const int row = s_row[i];
+        if (row < 0) continue;
+        const int64_t q = p0 + i;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (q / k) * d);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)row * d);
+        if (SCALE) {
+            const float wq = scale[q];
+            for (int v = lane; v < nvec; v += 32) {
+                float f[EPV];
+                unpack16(ldg16(src + v), f, static_cast<const TA *>(nullptr));
 #pragma unroll
-        for (int i = 0; i < EPV; ++i) f[i] *= wq;
-        stg16(dst + (int64_t)v * EPV, pack16(f, static_cast<const TA *>(nullptr)));
+                for (int j = 0; j < EPV; ++j) f[j] *= wq;
+                stg16(dst + v, pack16(f, static_cast<const TA *>(nullptr)));
+            }
+            continue;
+        }
+        int v = lane;
+        for (; v + 96 < nvec; v += 128) {
+            const uint4 a = ldg16(src + v), b = ldg16(src + v + 32), c = ldg16(src + v + 64),
+                        dd = ldg16(src + v + 96);
+            stg16(dst + v, a);
+            stg16(dst + v + 32, b);
+            stg16(dst + v + 64, c);
+            stg16(dst + v + 96, dd);
+        }
+        for (; v < nvec; v += 32) stg16(dst + v, ldg16(src + v));
     }
 }
 
@@ -238,47 +260,77 @@ DispatchGrid dispatch_grid(int64_t P, int E) {
     return g;
 }
 
+// The count matrix [E][chunks] and, after it, the rank kernel's ticket.
 size_t dispatch_scratch_bytes(const Shape &s) {
     DispatchGrid g = dispatch_grid(s.P(), s.E);
-    return sizeof(int32_t) * (size_t)s.E * (size_t)g.blocks;
+    return sizeof(int32_t) * (size_t)s.E * (size_t)g.blocks + 16;
+}
+
+unsigned *dispatch_ticket(const Shape &s, int32_t *scratch) {
+    DispatchGrid g = dispatch_grid(s.P(), s.E);
+    return reinterpret_cast<unsigned *>(scratch + (size_t)s.E * (size_t)g.blocks);
+}
+
+// Pairs per place_rows_kernel block: about P / 2048 (so ~2048 blocks), a
+// power of two from 8 to 256 that divides the chunk (a multiple of 256).
+int place_group(int64_t P) {
+    int g = 8;
+    while (g < 256 && (int64_t)g * 2048 < P) g *= 2;
+    return g;
 }
 
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
-                            const float *scale) {
+                            const float *scale, bool ticket_zeroed) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {  // E = 1024: 32 warps x 1024 counts = 128 KB
+        if ((err = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kRankWarps * 1024 * (int)sizeof(int))) != cudaSuccess)
+            return err;
+        attr_set[dev] = true;
+    }
     const int64_t P = s.P();
     const DispatchGrid g = dispatch_grid(P, s.E);
-    launch_pdl(chunk_histogram_kernel, dim3(g.blocks), dim3(kThreads), sizeof(int) * s.E, st, idx, P, s.E, g.chunk,
-                                                                        g.blocks, hist, ds);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
+    unsigned *ticket = dispatch_ticket(s, hist);
+    if (!ticket_zeroed && (err = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st)) != cudaSuccess)
+        return err;
     const int64_t n_hist = (int64_t)s.E * g.blocks;
-    if (n_hist <= kScanStageMax)
-        launch_pdl(scan_kernel<true>, dim3(1), dim3(kScanThreads), sizeof(int) * (size_t)n_hist, st,
-                   hist, s.E, g.blocks, counts, offsets);
-    else
-        launch_pdl(scan_kernel<false>, dim3(1), dim3(kScanThreads), 0, st, hist, s.E, g.blocks,
-                   counts, offsets);
+    const int staged = n_hist <= kScanStageMax ? 1 : 0;
+    const size_t sh = sizeof(int) * (size_t)std::max<int64_t>((int64_t)kRankWarps * s.E,
+                                                               staged ? n_hist : 0);
+    launch_pdl(rank_kernel, dim3(g.blocks), dim3(kRankThreads), sh, st, idx, P, s.E, g.chunk,
+               g.blocks, staged, hist, pos, counts, offsets, ticket, ds);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const size_t sh = sizeof(int) * (size_t)kWarps * s.E;
-    launch_pdl(scatter_kernel, dim3(g.blocks), dim3(kThreads), sh, st, idx, P, s.k, s.E, g.chunk, g.blocks, hist, pos,
-                                                  src_token);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (!x_perm) return cudaSuccess;
-    const int row_vecs = (int)((int64_t)s.d * (s.bf16 ? 2 : 4) / 16);
-    const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
-    if (scale && s.bf16)
-        launch_pdl(gather_rows_scaled_kernel<__nv_bfloat16>, dim3(blocks), dim3(kThreads), 0, st,
-            static_cast<const __nv_bfloat16 *>(x), pos, scale, P, s.k, s.d,
-            static_cast<__nv_bfloat16 *>(x_perm));
-    else if (scale)
-        launch_pdl(gather_rows_scaled_kernel<float>, dim3(blocks), dim3(kThreads), 0, st,
-            static_cast<const float *>(x), pos, scale, P, s.k, s.d, static_cast<float *>(x_perm));
-    else
-        launch_pdl(gather_rows_kernel, dim3(blocks), dim3(kThreads), 0, st, static_cast<const uint8_t *>(x), pos, P,
-                                                       s.k, row_vecs,
-                                                       static_cast<uint8_t *>(x_perm));
+    const int G = place_group(P);
+    const unsigned blocks = (unsigned)((P + G - 1) / G);
+    const int32_t *chist = hist;
+    if (s.bf16) {
+        using T = __nv_bfloat16;
+        const T *xt = static_cast<const T *>(x);
+        T *xp = static_cast<T *>(x_perm);
+        if (scale && x_perm)
+            launch_pdl(place_rows_kernel<T, true>, dim3(blocks), dim3(kThreads), 0, st, xt, chist,
+                       scale, P, s.k, s.d, g.chunk, g.blocks, G, pos, src_token, xp);
+        else
+            launch_pdl(place_rows_kernel<T, false>, dim3(blocks), dim3(kThreads), 0, st, xt, chist,
+                       (const float *)nullptr, P, s.k, s.d, g.chunk, g.blocks, G, pos, src_token,
+                       xp);
+    } else {
+        const float *xt = static_cast<const float *>(x);
+        float *xp = static_cast<float *>(x_perm);
+        if (scale && x_perm)
+            launch_pdl(place_rows_kernel<float, true>, dim3(blocks), dim3(kThreads), 0, st, xt,
+                       chist, scale, P, s.k, s.d, g.chunk, g.blocks, G, pos, src_token, xp);
+        else
+            launch_pdl(place_rows_kernel<float, false>, dim3(blocks), dim3(kThreads), 0, st, xt,
+                       chist, (const float *)nullptr, P, s.k, s.d, g.chunk, g.blocks, G, pos,
+                       src_token, xp);
+    }
     return cudaGetLastError();
 }
 

@@ -1,7 +1,7 @@
 // dispatch_noalloc.cu -- moe_dispatch for callers that cannot allocate.
 //
-// moe_dispatch needs a small scratch buffer (per-chunk expert histograms)
-// that its caller normally provides.  Some callers have no way to provide it:
+// moe_dispatch needs a small scratch buffer (per-chunk expert counts and a
+// ticket counter) that its caller normally provides.  Some callers have no way to provide it:
 // a plugin inside a host framework that owns all device memory and hands the
 // layer only its inputs and outputs, or a service that must not call
 // cudaMalloc once it has started serving (its allocations are fixed at
@@ -14,10 +14,12 @@
 // use of the device) until the process exits.  The device address is looked
 // up once per device and kept: a device reset after the first call is not
 // supported.  Every call on a device shares it and it keeps the last call's
-// contents; nothing in it needs to start at zero, because the histogram
-// kernel writes every entry a call reads before the scan reads it.  Calls
-// whose kernels overlap on the GPU (other streams, other threads) race on
-// the array and must be serialised by the caller.
+// contents.  The one word that must start at zero, the ticket counter, is
+// cleared by every call (a 4-byte cudaMemsetAsync on the caller's stream,
+// which allocates nothing) before its kernels; the counts are all written
+// before they are read.  Calls whose kernels overlap on the GPU (other
+// streams, other threads) race on the array and must be serialised by the
+// caller.
 #include <mutex>
 
 #include "moe.h"
@@ -25,7 +27,8 @@
 
 namespace {
 
-// 1 MiB of int32 histogram entries: E * chunks <= 262,144.
+// 1 MiB: the E x chunks int32 count matrix (E * chunks <= 262,140) and the
+// 16-byte ticket after it.
 constexpr size_t kNoAllocScratchInts = (size_t)1 << 18;
 constexpr size_t kNoAllocScratchBytes = kNoAllocScratchInts * sizeof(int32_t);
 
@@ -44,8 +47,9 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t *cfg, const int3
     const size_t need = moe_dispatch_workspace_size(cfg);
     if (need > kNoAllocScratchBytes) {
         moe::set_error_message(
-            "moe_dispatch_noalloc: this call needs %zu bytes of histogram scratch (E * chunks "
-            "ints); the static array holds %zu bytes. Use moe_dispatch with a caller buffer.",
+            "moe_dispatch_noalloc: this call needs %zu bytes of dispatch scratch (E * chunks "
+            "ints and a ticket); the static array holds %zu bytes. Use moe_dispatch with a caller "
+            "buffer.",
             need, kNoAllocScratchBytes);
         return MOE_ERR_UNSUPPORTED;
     }

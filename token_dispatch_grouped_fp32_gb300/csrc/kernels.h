@@ -20,18 +20,22 @@ struct Shape {
 // Router: logits[T][E] = x @ Wr^T (+ bias), fp32 accumulation.  When
 // router_selects_in_logits(s) and idx/w are given, the same launch also
 // writes the top-k selection and weights (no separate top-k launch).
+// zero_word (optional, for the selecting launches here and below): a word
+// the launch sets to 0, so a later kernel in the stream finds it cleared
+// (the dispatch's ticket counter).
 cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr,
                                  const float *bias, float *logits, cudaStream_t st,
-                                 int32_t *idx = nullptr, float *w = nullptr);
+                                 int32_t *idx = nullptr, float *w = nullptr,
+                                 unsigned *zero_word = nullptr);
 bool router_selects_in_logits(const Shape &s);
 // Top-k selection and softmax weights on a given fp32 logit buffer.
 cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
-                        cudaStream_t st);
+                        cudaStream_t st, unsigned *zero_word = nullptr);
 // Top-k on logits formed as sum of `splits` partial buffers [splits][T][E]
 // (added in split order) plus bias; the logits are written to `logits`.
 cudaError_t launch_topk_partials(const Shape &s, const float *partial, int splits,
                                  const float *bias, float *logits, int32_t *idx, float *w,
-                                 cudaStream_t st);
+                                 cudaStream_t st, unsigned *zero_word = nullptr);
 
 // Router logits on the tensor cores (bf16 x, fp32 Wr split into 3 bf16 terms).
 struct RouterTcPlan {
@@ -47,19 +51,24 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
                                     float **partial_out, int *splits_out, const DevStatus &ds,
                                     cudaStream_t st);
 
-// Dispatch: chunking of the P pairs over histogram/scatter blocks.
+// Dispatch: chunking of the P pairs over the rank kernel's blocks.
 struct DispatchGrid {
     int chunk;  // pairs per block (multiple of 256)
     int blocks;  // number of blocks (>= 1 when P > 0)
 };
 DispatchGrid dispatch_grid(int64_t P, int E);
-size_t dispatch_scratch_bytes(const Shape &s);  // per-block histogram ints
+size_t dispatch_scratch_bytes(const Shape &s);  // count matrix [E][chunks] + ticket
+// The ticket counter inside the dispatch scratch `hist` (must be 0 when the
+// dispatch's first launch starts; the dispatch leaves it 0).
+unsigned *dispatch_ticket(const Shape &s, int32_t *hist);
 // x_perm == nullptr: counts, offsets, pos and src_token only (no row gather).
 // scale != nullptr: each gathered row is multiplied by its pair's weight.
+// ticket_zeroed: an earlier kernel in the stream already cleared the ticket;
+// otherwise it is cleared here with a 4-byte cudaMemsetAsync.
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
-                            const float *scale = nullptr);
+                            const float *scale = nullptr, bool ticket_zeroed = false);
 
 // Grouped SwiGLU experts.  bf16: tcgen05 tensor-core path; fp32: SIMT path.
 // Kernel launches of one launch_grouped_swiglu_tc call (2, or 4 when the

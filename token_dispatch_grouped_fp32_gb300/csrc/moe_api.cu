@@ -204,9 +204,11 @@ template <typename T> T *at(void *ws, size_t off) {
 
 // Router: tensor-core logits (split weight, K-split partials summed by the
 // top-k kernel) when the shape allows, else the SIMT logits kernel.
+// zero_word (optional): cleared by the route's last launch (the dispatch's
+// ticket, when moe_forward runs the dispatch next).
 moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const float *bias,
                        float *logits, int32_t *idx, float *w, void *route_ws,
-                       const DevStatus &ds, cudaStream_t st) {
+                       const DevStatus &ds, cudaStream_t st, unsigned *zero_word = nullptr) {
     if (router_tc_eligible(s)) {
         float *partial = nullptr;
         int splits = 0;
@@ -214,16 +216,17 @@ moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const flo
             launch_router_logits_tc(s, x, Wr, route_ws, &partial, &splits, ds, st),
             "router logits launch");
         if (r != MOE_OK) return r;
-        return from_cuda(launch_topk_partials(s, partial, splits, bias, logits, idx, w, st),
-                         "top-k launch");
+        return from_cuda(
+            launch_topk_partials(s, partial, splits, bias, logits, idx, w, st, zero_word),
+            "top-k launch");
     }
     if (router_selects_in_logits(s))  // one launch: logits, selection and weights
-        return from_cuda(launch_router_logits(s, x, Wr, bias, logits, st, idx, w),
+        return from_cuda(launch_router_logits(s, x, Wr, bias, logits, st, idx, w, zero_word),
                          "router launch");
     moe_status_t r = from_cuda(launch_router_logits(s, x, Wr, bias, logits, st),
                                "router logits launch");
     if (r != MOE_OK) return r;
-    return from_cuda(launch_topk(s, logits, idx, w, st), "top-k launch");
+    return from_cuda(launch_topk(s, logits, idx, w, st, zero_word), "top-k launch");
 }
 
 moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offsets,
@@ -314,7 +317,7 @@ int moe_forward_kernel_launches(const moe_config_t *cfg) {
     // CUDA cores selecting in the logits launch, or CUDA-core logits + top-k
     const int route = router_tc_eligible(s) ? 3 : router_selects_in_logits(s) ? 1 : 2;
     const int experts = s.bf16 ? grouped_swiglu_tc_launches(s) : 2 /* G1, G2 */;
-    return route + 4 /* histogram, scan, scatter, gather */ + experts + 1 /* combine */;
+    return route + 2 /* rank (with the count scan), place rows */ + experts + 1 /* combine */;
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) {
@@ -454,12 +457,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
     void *x_perm = at<uint8_t>(ws, L.x_perm), *h_perm = at<uint8_t>(ws, L.h_perm),
          *y_perm = at<uint8_t>(ws, L.y_perm);
 
-    if ((st = run_route(s, x, Wr, logit_bias, logits, idx, w, at<uint8_t>(ws, L.route), ds, cs)) !=
-        MOE_OK)
+    int32_t *hist = at<int32_t>(ws, L.hist);
+    // the route's last launch clears the dispatch's ticket counter
+    if ((st = run_route(s, x, Wr, logit_bias, logits, idx, w, at<uint8_t>(ws, L.route), ds, cs,
+                        dispatch_ticket(s, hist))) != MOE_OK)
         return st;
-    if ((st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm,
-                                        at<int32_t>(ws, L.hist), ds, cs,
-                                        s.scale_inputs ? w : nullptr),
+    if ((st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm, hist, ds, cs,
+                                        s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true),
                         "dispatch launch")) != MOE_OK)
         return st;
     if ((st = run_experts(s, x_perm, offsets, W_gate_up, W_down, h_perm, y_perm, ds, cs)) != MOE_OK)

@@ -74,8 +74,11 @@ __global__ void __launch_bounds__(256)
 router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
                            const float *__restrict__ bias, float *__restrict__ logits,
                            int64_t T, int d, int E, int k, int renorm,
-                           int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+                           int32_t *__restrict__ topk_idx, float *__restrict__ topk_w,
+                           unsigned *__restrict__ zero_word) {
     pdl_entry();
+    if (zero_word != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        *zero_word = 0u;
     constexpr int TPW = 32 / EP;
     __shared__ float red[kSplitWarps][32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -294,7 +297,8 @@ cudaError_t launch_logits_cfg(const Shape &s, const TA *x, const float *Wr, cons
 
 template <typename TA, int EP>
 cudaError_t launch_logits_split(const Shape &s, const TA *x, const float *Wr, const float *bias,
-                                float *logits, int32_t *idx, float *w, cudaStream_t st) {
+                                float *logits, int32_t *idx, float *w, cudaStream_t st,
+                                unsigned *zero_word) {
     constexpr int TPW = 32 / EP;
     dim3 grid((unsigned)((s.T + TPW - 1) / TPW), (unsigned)((s.E + EP - 1) / EP));
     // with a single expert group (E <= 32) the kernel also selects; larger E
@@ -302,22 +306,23 @@ cudaError_t launch_logits_split(const Shape &s, const TA *x, const float *Wr, co
     const bool fused = grid.y == 1 && idx != nullptr;
     launch_pdl(router_logits_split_kernel<TA, EP>, dim3(grid), dim3(256), 0, st,
         x, Wr, bias, logits, s.T, s.d, s.E, s.k, s.renorm ? 1 : 0, fused ? idx : nullptr,
-        fused ? w : nullptr);
+        fused ? w : nullptr, fused ? zero_word : nullptr);
     return cudaGetLastError();
 }
 
 template <typename TA>
 cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const float *bias,
-                            float *logits, int32_t *idx, float *w, cudaStream_t st) {
-    if (s.E <= 1) return launch_logits_split<TA, 1>(s, x, Wr, bias, logits, idx, w, st);
-    if (s.E <= 2) return launch_logits_split<TA, 2>(s, x, Wr, bias, logits, idx, w, st);
-    if (s.E <= 4) return launch_logits_split<TA, 4>(s, x, Wr, bias, logits, idx, w, st);
-    if (s.E <= 8) return launch_logits_split<TA, 8>(s, x, Wr, bias, logits, idx, w, st);
-    if (s.E <= 16) return launch_logits_split<TA, 16>(s, x, Wr, bias, logits, idx, w, st);
-    if (s.E <= 32) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, idx, w, st);
+                            float *logits, int32_t *idx, float *w, cudaStream_t st,
+                            unsigned *zero_word) {
+    if (s.E <= 1) return launch_logits_split<TA, 1>(s, x, Wr, bias, logits, idx, w, st, zero_word);
+    if (s.E <= 2) return launch_logits_split<TA, 2>(s, x, Wr, bias, logits, idx, w, st, zero_word);
+    if (s.E <= 4) return launch_logits_split<TA, 4>(s, x, Wr, bias, logits, idx, w, st, zero_word);
+    if (s.E <= 8) return launch_logits_split<TA, 8>(s, x, Wr, bias, logits, idx, w, st, zero_word);
+    if (s.E <= 16) return launch_logits_split<TA, 16>(s, x, Wr, bias, logits, idx, w, st, zero_word);
+    if (s.E <= 32) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, idx, w, st, zero_word);
     // larger E: the tiled kernel re-reads Wr far less per token, but needs
     // enough row tiles to fill the GPU; small batches use 32-expert groups.
-    if (s.T < 2048) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, idx, w, st);
+    if (s.T < 2048) return launch_logits_split<TA, 32>(s, x, Wr, bias, logits, idx, w, st, zero_word);
     if (s.E <= 64) return launch_logits_cfg<TA, 64, 64, 4, 4>(s, x, Wr, bias, logits, st);
     return launch_logits_cfg<TA, 64, 128, 4, 8>(s, x, Wr, bias, logits, st);
 }
@@ -352,8 +357,9 @@ template <int VPL>
 __global__ void __launch_bounds__(256)
 topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int nparts,
             const float *__restrict__ bias, int64_t T, int E, int k, int renorm,
-            int32_t *__restrict__ idx, float *__restrict__ w) {
+            int32_t *__restrict__ idx, float *__restrict__ w, unsigned *__restrict__ zero_word) {
     pdl_entry();
+    if (zero_word != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0u;
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;  // warp-uniform
@@ -444,45 +450,50 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
 
 template <int VPL>
 cudaError_t launch_topk_v(const Shape &s, float *logits, const float *partial, int nparts,
-                          const float *bias, int32_t *idx, float *w, cudaStream_t st) {
+                          const float *bias, int32_t *idx, float *w, cudaStream_t st,
+                          unsigned *zero_word) {
     unsigned blocks = (unsigned)((s.T + 7) / 8);
-    launch_pdl(topk_kernel<VPL>, dim3(blocks), dim3(256), 0, st, logits, partial, nparts, bias, s.T, s.E, s.k,
-                                             s.renorm ? 1 : 0, idx, w);
+    launch_pdl(topk_kernel<VPL>, dim3(blocks), dim3(256), 0, st, logits, partial, nparts, bias, s.T,
+               s.E, s.k, s.renorm ? 1 : 0, idx, w, zero_word);
     return cudaGetLastError();
 }
 
 cudaError_t launch_topk_any(const Shape &s, float *logits, const float *partial, int nparts,
-                            const float *bias, int32_t *idx, float *w, cudaStream_t st) {
-    if (s.E <= 32) return launch_topk_v<1>(s, logits, partial, nparts, bias, idx, w, st);
-    if (s.E <= 64) return launch_topk_v<2>(s, logits, partial, nparts, bias, idx, w, st);
-    if (s.E <= 128) return launch_topk_v<4>(s, logits, partial, nparts, bias, idx, w, st);
-    if (s.E <= 256) return launch_topk_v<8>(s, logits, partial, nparts, bias, idx, w, st);
-    if (s.E <= 512) return launch_topk_v<16>(s, logits, partial, nparts, bias, idx, w, st);
-    return launch_topk_v<32>(s, logits, partial, nparts, bias, idx, w, st);
+                            const float *bias, int32_t *idx, float *w, cudaStream_t st,
+                            unsigned *zero_word) {
+    if (s.E <= 32) return launch_topk_v<1>(s, logits, partial, nparts, bias, idx, w, st, zero_word);
+    if (s.E <= 64) return launch_topk_v<2>(s, logits, partial, nparts, bias, idx, w, st, zero_word);
+    if (s.E <= 128) return launch_topk_v<4>(s, logits, partial, nparts, bias, idx, w, st, zero_word);
+    if (s.E <= 256) return launch_topk_v<8>(s, logits, partial, nparts, bias, idx, w, st, zero_word);
+    if (s.E <= 512) return launch_topk_v<16>(s, logits, partial, nparts, bias, idx, w, st, zero_word);
+    return launch_topk_v<32>(s, logits, partial, nparts, bias, idx, w, st, zero_word);
 }
 
 }  // namespace
 
 cudaError_t launch_router_logits(const Shape &s, const void *x, const float *Wr, const float *bias,
-                                 float *logits, cudaStream_t st, int32_t *idx, float *w) {
+                                 float *logits, cudaStream_t st, int32_t *idx, float *w,
+                                 unsigned *zero_word) {
     if (s.bf16)
         return launch_logits_t<__nv_bfloat16>(s, static_cast<const __nv_bfloat16 *>(x), Wr, bias,
-                                              logits, idx, w, st);
-    return launch_logits_t<float>(s, static_cast<const float *>(x), Wr, bias, logits, idx, w, st);
+                                              logits, idx, w, st, zero_word);
+    return launch_logits_t<float>(s, static_cast<const float *>(x), Wr, bias, logits, idx, w, st,
+                                  zero_word);
 }
 
 bool router_selects_in_logits(const Shape &s) { return s.E <= 32; }
 
 cudaError_t launch_topk(const Shape &s, const float *logits, int32_t *idx, float *w,
-                        cudaStream_t st) {
+                        cudaStream_t st, unsigned *zero_word) {
     // nparts == 0: the kernel only reads `logits`
-    return launch_topk_any(s, const_cast<float *>(logits), nullptr, 0, nullptr, idx, w, st);
+    return launch_topk_any(s, const_cast<float *>(logits), nullptr, 0, nullptr, idx, w, st,
+                           zero_word);
 }
 
 cudaError_t launch_topk_partials(const Shape &s, const float *partial, int splits,
                                  const float *bias, float *logits, int32_t *idx, float *w,
-                                 cudaStream_t st) {
-    return launch_topk_any(s, logits, partial, splits, bias, idx, w, st);
+                                 cudaStream_t st, unsigned *zero_word) {
+    return launch_topk_any(s, logits, partial, splits, bias, idx, w, st, zero_word);
 }
 
 }  // namespace moe
