@@ -19,7 +19,7 @@ The line also carries: `roofline` (the grouped GEMM against the bf16 tensor
 peak: the burst figure, or the sustained one when the clocks sampled in the
 timed region show sw_power_cap), `layer_roofline` (the slower of the layer's
 FLOPs at that peak and its minimal HBM bytes at the HBM peak, against the
-step time), a per-kernel breakdown, and `all_workloads`: the other four
+step time), a per-kernel breakdown, and `all_workloads`: the other
 workloads timed the same way (K steps each, L2 flushed between steps).
 """
 from __future__ import annotations
@@ -39,7 +39,8 @@ if ROOT not in sys.path:
 METRIC = "MoE-layer tokens/s on 1 GB300; GEMM % tensor peak, permute/combine % HBM BW"
 # every bf16 workload of the benchmark; the one named by --workload (default
 # mixtral) is the headline line, the others go in its all_workloads block
-ALL_WORKLOADS = ["mixtral", "gptoss_decode", "gptoss_prefill", "qwen3_zipf", "deepseek"]
+ALL_WORKLOADS = ["mixtral", "gptoss_decode", "gptoss_prefill", "qwen3_zipf", "deepseek",
+                 "mixtral_norenorm", "mixtral_dense"]
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -253,11 +254,18 @@ def workload_config(w):
 # --------------------------------------------------------------------------
 def gemm_peak(peaks, clocks):
     """The bf16 tensor peak the timed GEMM is held to: the sustained
-    (power-capped) figure when sw_power_cap was active under load during the
-    timed region, else the burst figure."""
-    if "sw_power_cap" in (clocks.get("reasons") or []) and peaks.get("bf16_tflops_sustained"):
-        return peaks["bf16_tflops_sustained"], "bf16_tflops_sustained (sw_power_cap active under load)"
-    return peaks["bf16_tflops"], "bf16_tflops (burst: no power cap under load)"
+    (power-capped) figure when the power cap actually held the clock down in
+    the timed region (sw_power_cap active under load and the median SM clock
+    below 97 % of its maximum), else the burst figure.  (nvidia-smi can show
+    sw_power_cap active while the clock stays at its maximum.)"""
+    reasons = clocks.get("reasons") or []
+    sm, sm_max = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    held = sm is not None and sm_max and sm < 0.97 * sm_max
+    if "sw_power_cap" in reasons and held and peaks.get("bf16_tflops_sustained"):
+        return (peaks["bf16_tflops_sustained"],
+                f"bf16_tflops_sustained (sw_power_cap held the clock at {sm:.0f} MHz)")
+    note = "sw_power_cap shown, clock at maximum" if "sw_power_cap" in reasons else "no power cap"
+    return peaks["bf16_tflops"], f"bf16_tflops (burst: {note})"
 
 
 def layer_roofline(w, touched, ms, peaks, tflops_peak):

@@ -110,8 +110,9 @@ size_t moe_workspace_size(const moe_config_t *cfg);
  *   pos       int32 [P],     src_token int32 [P]   (as moe_dispatch defines them)
  *   x_perm    act [P][d],    h_perm act [P][f],    y_perm act [P][d]
  *   total     = moe_workspace_size(cfg)
- * Any other bytes of the workspace are library scratch.  T == 0 gives all
- * zeros.  Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a config
+ * Any other bytes of the workspace are library scratch.  With k == E and
+ * the weights on the outputs (scale_inputs == 0), x_perm is not written: the
+ * experts read x directly (see moe_forward).  T == 0 gives all zeros.  Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a config
  * moe_forward would reject, or a NULL `layout`.  Launches nothing (it only
  * queries the current device's SM count, as moe_workspace_size does).
  */
@@ -129,7 +130,8 @@ size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
 
 /*
  * Number of kernel launches one moe_forward call makes for `cfg`: the router
- * (1 to 3 launches, by path), the dispatch (2), the two grouped GEMMs (2, or
+ * (1 to 3 launches, by path), the dispatch (2; 1 when k == E without
+ * scale_inputs), the two grouped GEMMs (2, or
  * 4 when bf16 experts average 64 to 511 rows each and are split between two
  * tile shapes) and the combine (1).  0 when T == 0; -1 for an invalid
  * configuration.  Makes no CUDA call.
@@ -271,6 +273,11 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm,
 /*
  * The whole layer, one stream, no host synchronisation: moe_route,
  * moe_dispatch, moe_grouped_swiglu, moe_combine.
+ * When k == E and the weights act on the outputs (scale_inputs == 0), every
+ * expert receives every token unscaled, so there is nothing to permute
+ * [EP]: expert e's segment is rows e*T .. e*T + T-1 in token order, the
+ * dispatch only writes counts, offsets, pos and src_token, and the first
+ * grouped GEMM reads the rows of x itself instead of x_perm.
  * x [T][d], Wr [E][d] fp32, logit_bias [E] fp32 or NULL,
  * W_gate_up [E][d][2f], W_down [E][f][d], out [T][d] (written).
  * ws: at least moe_workspace_size(cfg) bytes, 256-byte aligned; its

@@ -158,6 +158,10 @@ def test_forward_kernel_launches(moe):
     assert moe.moe_forward_kernel_launches(moe.config(64, 128, 8, 2, 256, "f32")) == 6
     # fp32 activations, E > 32: CUDA-core logits, then the top-k kernel
     assert moe.moe_forward_kernel_launches(moe.config(4096, 128, 64, 2, 256, "f32")) == 7
+    # k = E (weights on the outputs): one dispatch launch, no permutation
+    assert moe.moe_forward_kernel_launches(moe.config(1024, 4096, 8, 8, 14336, "bf16", False)) == 7
+    assert moe.moe_forward_kernel_launches(
+        moe.config(1024, 4096, 8, 8, 14336, "bf16", False, scale_inputs=True)) == 8
     assert moe.moe_forward_kernel_launches(moe.config(0, 128, 8, 2, 256, "bf16")) == 0
     assert moe.moe_forward_kernel_launches(moe.config(4, 4096, 8, 9, 14336)) == -1
 

@@ -37,3 +37,32 @@ def test_warmup_below_three_is_rejected():
     r = _run("--impl", "reference", "--workload", "tiny_fp32", "--steps", "2", "--warmup", "1")
     assert r.returncode != 0
     assert "warmup" in r.stderr
+
+
+def test_gemm_peak_follows_the_sampled_clocks():
+    """Burst peak unless the power cap actually held the SM clock down."""
+    import bench
+    pk = {"hbm_gbs": 6777.0, "bf16_tflops": 1919.4, "bf16_tflops_sustained": 1711.7}
+    assert bench.gemm_peak(pk, {"reasons": [], "sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == 1919.4
+    assert bench.gemm_peak(pk, {"reasons": ["sw_power_cap"], "sm_mhz": 2070.0,
+                                "sm_max_mhz": 2070.0})[0] == 1919.4
+    assert bench.gemm_peak(pk, {"reasons": ["sw_power_cap"], "sm_mhz": 1500.0,
+                                "sm_max_mhz": 2070.0})[0] == 1711.7
+
+
+def test_layer_roofline_is_the_slower_bound():
+    """FLOPs 2TdE + 6Pdf at the tensor peak against the touched experts'
+    weights + x + out + Wr at the HBM peak; the slower decides."""
+    import bench
+    from token_dispatch_grouped_fp32_gb300 import synth
+    pk = {"hbm_gbs": 6777.0}
+    w = synth.WORKLOADS["mixtral"]
+    r = bench.layer_roofline(w, 8, 1.8, pk, 1919.4)
+    flops = 2 * 4096 * 4096 * 8 + 6 * 8192 * 4096 * 14336
+    assert r["flops"] == flops and r["bound"] == "tensor"
+    assert abs(r["frac"] - flops / 1919.4e12 / 1.8e-3) < 1e-12
+    d = synth.WORKLOADS["gptoss_decode"]
+    r = bench.layer_roofline(d, 111, 0.85, pk, 1919.4)
+    nbytes = 111 * 3 * 2880 * 2880 * 2 + 2 * 64 * 2880 * 2 + 4 * 128 * 2880
+    assert r["bytes"] == nbytes and r["bound"] == "hbm"
+    assert abs(r["frac"] - nbytes / 6777e9 / 0.85e-3) < 1e-12

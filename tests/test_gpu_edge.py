@@ -26,10 +26,61 @@ def test_one_expert(moe, oracle, dtype):
     check_layer(moe, oracle, w, device="cpu")
 
 
+@pytest.mark.parametrize("renorm", [False, True])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_k_equals_E_without_renorm(moe, oracle, dtype):
-    w = synth.Workload("dense", 200, 96, 4, 4, 136, dtype, 22, renorm=False)
+def test_k_equals_E(moe, oracle, dtype, renorm):
+    """k = E: the path with nothing to permute (the experts read x itself)."""
+    w = synth.Workload("dense", 200, 96, 4, 4, 136, dtype, 22, renorm=renorm)
     check_layer(moe, oracle, w, device="cpu")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T,E", [(300, 8), (1000, 16), (77, 2)])
+def test_all_experts_path_equals_routed_components(moe, dtype, T, E):
+    """k = E: moe_forward's path without the permutation gives the same bits
+    as the component calls (route, the general dispatch with its row copy,
+    grouped GEMMs, combine), and its dispatch arrays are the identity order:
+    expert e's segment is the T tokens in order."""
+    w = synth.Workload("allexp", T, 128, E, E, 200, dtype, 40 + E, renorm=False)
+    inp = synth.make_inputs(w, device="cuda")
+    layer = moe.MoELayer(inp["Wr"], inp["Wgu"], inp["Wd"], E, None, False)
+    x = inp["x"]
+    out = layer(x)
+    cfg = layer.config(T)
+    L = moe.moe_workspace_layout(cfg)
+    ws = layer.workspace(T)
+    P = T * E
+    idx = ws[L.topk_idx:L.topk_idx + 4 * P].view(torch.int32).view(T, E).clone()
+    pos = ws[L.pos:L.pos + 4 * P].view(torch.int32).clone()
+    src = ws[L.src_token:L.src_token + 4 * P].view(torch.int32).clone()
+    counts = ws[L.counts:L.counts + 4 * E].view(torch.int32).clone()
+    t_of = torch.arange(T, device="cuda", dtype=torch.int32)[:, None]
+    assert torch.equal(pos.view(T, E), idx * T + t_of)
+    assert torch.equal(src, torch.arange(T, device="cuda", dtype=torch.int32).repeat(E))
+    assert (counts == T).all()
+    # the general path through the component entry points
+    wt = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    idx2 = torch.empty(T, E, dtype=torch.int32, device="cuda")
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    rws = torch.empty(max(256, moe.moe_route_workspace_size(cfg)), dtype=torch.uint8, device="cuda")
+    moe.moe_route(cfg, x, inp["Wr"], None, logits, idx2, wt, rws)
+    cnt = torch.empty(E, dtype=torch.int32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    pos2 = torch.empty(P, dtype=torch.int32, device="cuda")
+    src2 = torch.empty(P, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty(P, w.d, dtype=x.dtype, device="cuda")
+    h_perm = torch.empty(P, w.f, dtype=x.dtype, device="cuda")
+    y_perm = torch.empty(P, w.d, dtype=x.dtype, device="cuda")
+    dws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8,
+                      device="cuda")
+    moe.moe_dispatch(cfg, idx2, wt, x, cnt, off, pos2, src2, x_perm, dws)
+    moe.moe_grouped_swiglu(cfg, x_perm, off, inp["Wgu"], inp["Wd"], h_perm, y_perm)
+    out2 = torch.empty_like(x)
+    moe.moe_combine(cfg, y_perm, pos2, wt, out2)
+    torch.cuda.synchronize()
+    assert moe.moe_last_device_error() == moe.MOE_OK
+    assert torch.equal(pos, pos2) and torch.equal(src, src2)
+    assert torch.equal(out, out2)
 
 
 def test_every_token_on_one_expert(moe, oracle):

@@ -28,7 +28,8 @@ from tests.gpu_util import f32, layer_tolerance, load_moe, logit_tolerance, weig
 
 pytestmark = pytest.mark.gpu
 
-WORKLOADS = ["mixtral", "gptoss_decode", "gptoss_prefill", "qwen3_zipf", "deepseek"]
+WORKLOADS = ["mixtral", "gptoss_decode", "gptoss_prefill", "qwen3_zipf", "deepseek",
+             "mixtral_norenorm", "mixtral_dense"]
 
 
 @pytest.fixture(scope="module")
@@ -100,9 +101,13 @@ def test_full_size_routing_and_dispatch(oracle, run):
     np.testing.assert_array_equal(r["pos"].cpu().numpy(), rp)
     np.testing.assert_array_equal(r["src"].cpu().numpy(), rs)
     assert rc.sum() == w.T * w.k
-    # permuted rows are byte copies of the token rows
-    src = torch.from_numpy(rs).long().cuda()
-    assert torch.equal(r["x_perm"], r["inp"]["x"][src])
+    # permuted rows are byte copies of the token rows (k == E: the experts
+    # read x itself, and each segment holds the tokens in order)
+    if w.k == w.E:
+        np.testing.assert_array_equal(rs, np.tile(np.arange(w.T), w.E))
+    else:
+        src = torch.from_numpy(rs).long().cuda()
+        assert torch.equal(r["x_perm"], r["inp"]["x"][src])
 
 
 def _rows_to_check(count, rng):

@@ -239,7 +239,47 @@ place_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist,
     }
 }
 
+// Every token picks every expert (k == E), each once, so expert e's segment
+// is the T tokens in order: the row of pair q = (t, j) is idx[q] * T + t.
+__global__ void __launch_bounds__(kThreads)
+dispatch_all_experts_kernel(const int32_t *__restrict__ idx, int64_t T, int E,
+                            int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                            int32_t *__restrict__ pos, int32_t *__restrict__ src_token,
+                            DevStatus ds) {
+    pdl_entry();
+    const int64_t P = T * E;
+    if (blockIdx.x == 0) {
+        for (int e = threadIdx.x; e <= E; e += kThreads) {
+            offsets[e] = (int32_t)(e * T);
+            if (e < E) counts[e] = (int32_t)T;
+        }
+    }
+    for (int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x; q < P;
+         q += (int64_t)gridDim.x * kThreads) {
+        const int e = idx[q];
+        const int64_t t = q / E;
+        if ((unsigned)e >= (unsigned)E) {
+            raise_error(ds, kErrBadRouting);
+            pos[q] = -1;
+            continue;
+        }
+        const int64_t row = (int64_t)e * T + t;
+        pos[q] = (int32_t)row;
+        src_token[row] = (int32_t)t;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dispatch_all_experts(const Shape &s, const int32_t *idx, int32_t *counts,
+                                        int32_t *offsets, int32_t *pos, int32_t *src_token,
+                                        const DevStatus &ds, cudaStream_t st) {
+    const int64_t P = s.P();
+    const unsigned blocks = (unsigned)std::min<int64_t>((P + kThreads - 1) / kThreads, 4096);
+    launch_pdl(dispatch_all_experts_kernel, dim3(blocks), dim3(kThreads), 0, st, idx, s.T, s.E,
+               counts, offsets, pos, src_token, ds);
+    return cudaGetLastError();
+}
 
 DispatchGrid dispatch_grid(int64_t P, int E) {
     // Chunks of 2048 pairs; 256 when the E x chunks histogram stays small

@@ -62,7 +62,7 @@ template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads)
 grouped_gemm_f32_kernel(const float *__restrict__ A, const int32_t *__restrict__ offsets, int E,
                         const float *__restrict__ B, int K, int Nb, int N, int f,
-                        float *__restrict__ C) {
+                        float *__restrict__ C, int a_local) {
     pdl_entry();
     extern __shared__ int s_dyn[];
     int *s_off = s_dyn;
@@ -77,6 +77,9 @@ grouped_gemm_f32_kernel(const float *__restrict__ A, const int32_t *__restrict__
     const int e = find_expert(s_tile, E, g);
     const int row0 = s_off[e] + (g - s_tile[e]) * BM;
     const int rows = min(BM, s_off[e + 1] - row0);
+    // a_local: A holds one row per position of the segment (row r of expert
+    // e reads A row r - offsets[e]), as when every expert sees every token
+    const int arow0 = a_local ? row0 - s_off[e] : row0;
     const int n0 = blockIdx.y * BN;
     const float *Be = B + (int64_t)e * K * Nb;
 
@@ -92,7 +95,7 @@ grouped_gemm_f32_kernel(const float *__restrict__ A, const int32_t *__restrict__
         for (int r = 0; r < (BM * BK) / kThreads; ++r) {
             int i = tid + r * kThreads;
             int m = i / BK, c = i % BK;
-            As[c][m] = (m < rows && k0 + c < K) ? A[(int64_t)(row0 + m) * K + k0 + c] : 0.f;
+            As[c][m] = (m < rows && k0 + c < K) ? A[(int64_t)(arow0 + m) * K + k0 + c] : 0.f;
         }
 #pragma unroll
         for (int r = 0; r < (BK * BN) / kThreads; ++r) {
@@ -143,18 +146,18 @@ grouped_gemm_f32_kernel(const float *__restrict__ A, const int32_t *__restrict__
 
 cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const int32_t *offsets,
                                       const float *Wgu, const float *Wd, float *h_perm,
-                                      float *y_perm, cudaStream_t st) {
+                                      float *y_perm, cudaStream_t st, bool a_local) {
     const int64_t P = s.P();
     const int64_t mtiles = (P + BM - 1) / BM + s.E;  // upper bound of sum_e ceil(count_e / BM)
     const size_t sh = sizeof(int) * (2 * (size_t)s.E + 2);
     dim3 g1((unsigned)mtiles, (unsigned)((s.f + BN - 1) / BN));
     launch_pdl(grouped_gemm_f32_kernel<true>, dim3(g1), dim3(kThreads), sh, st, x_perm, offsets, s.E, Wgu, s.d,
-                                                           2 * s.f, s.f, s.f, h_perm);
+                                                           2 * s.f, s.f, s.f, h_perm, a_local ? 1 : 0);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     dim3 g2((unsigned)mtiles, (unsigned)((s.d + BN - 1) / BN));
     launch_pdl(grouped_gemm_f32_kernel<false>, dim3(g2), dim3(kThreads), sh, st, h_perm, offsets, s.E, Wd, s.f, s.d,
-                                                            s.d, 0, y_perm);
+                                                            s.d, 0, y_perm, 0);
     return cudaGetLastError();
 }
 

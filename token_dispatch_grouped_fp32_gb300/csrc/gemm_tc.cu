@@ -126,6 +126,9 @@ struct Params {
     // B maps are the 64-column-block views (tensor_map_weight_blocks): one
     // box carries two 8 KB atoms
     int b_blocks;
+    // G1's A holds one row per position of a segment: row r of expert e
+    // reads A row r - offsets[e] (every expert sees every token, in order)
+    int a_local;
     DevStatus ds;
 };
 
@@ -331,7 +334,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                 int n0;
                 if (!ti.down) n0 = ti.n_blk * (BN / 2) + (PAIR && !leader ? p.f : 0);
                 else n0 = ti.n_blk * BN + (int)rank * (BN / 2);
-                const int arow = ti.row0 + (int)rank * BM;
+                const int arow = (p.a_local && !ti.down ? ti.row0 - s_off[ti.e] : ti.row0) +
+                                 (int)rank * BM;
                 const int nk = ti.down ? nk2 : nk1;
                 for (int ks = 0; ks < nk; ++ks) {
                     if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort)) {
@@ -670,7 +674,7 @@ int grouped_swiglu_tc_launches(const Shape &s) {
 
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
-                                     const DevStatus &ds, cudaStream_t st) {
+                                     const DevStatus &ds, cudaStream_t st, bool a_local) {
     using namespace tc;
     static DeviceInfo info[64];
     int dev = 0;
@@ -703,7 +707,8 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
                      tensor_map_weight_blocks(&mwd, Wd, s.E, s.f, s.d, 2)
                : tensor_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) &&
                      tensor_map_weights(&mwd, Wd, s.E, s.f, s.d);
-    if (!maps_ok || !tensor_map_rows(&mx, x_perm, P, s.d, BM) ||
+    // a_local: G1's A is the T token rows themselves
+    if (!maps_ok || !tensor_map_rows(&mx, x_perm, a_local ? s.T : P, s.d, BM) ||
         !tensor_map_rows(&mh, h_perm, P, s.f, BM)) {
         set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
         return cudaErrorInvalidValue;
@@ -731,6 +736,7 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     p.release_late = 0;
     p.overlap_prev = 0;
     p.b_blocks = blocks ? 1 : 0;
+    p.a_local = a_local ? 1 : 0;
     p.ds = ds;
     // G1 launches, then G2 launches (G2 reads h_perm; stream order)
     const TileMode mode = tile_mode(s);

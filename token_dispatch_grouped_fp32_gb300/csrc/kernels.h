@@ -74,12 +74,21 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
 // Kernel launches of one launch_grouped_swiglu_tc call (2, or 4 when the
 // experts are split between CTA-pair and single-CTA tiles).
 int grouped_swiglu_tc_launches(const Shape &s);
+// a_local: x_perm is the T token rows x, and row r of expert e's segment
+// reads row r - offsets[e] (every expert receives every token, in order).
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
-                                     const DevStatus &ds, cudaStream_t st);
+                                     const DevStatus &ds, cudaStream_t st, bool a_local = false);
 cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const int32_t *offsets,
                                       const float *Wgu, const float *Wd, float *h_perm,
-                                      float *y_perm, cudaStream_t st);
+                                      float *y_perm, cudaStream_t st, bool a_local = false);
+
+// Dispatch when every token picks every expert (k == E): counts[e] = T,
+// offsets[e] = e*T, pos[t*E+j] = idx[t][j]*T + t, src_token[e*T + t] = t.
+// No rows are copied (the experts read x with a_local).  One launch.
+cudaError_t launch_dispatch_all_experts(const Shape &s, const int32_t *idx, int32_t *counts,
+                                        int32_t *offsets, int32_t *pos, int32_t *src_token,
+                                        const DevStatus &ds, cudaStream_t st);
 
 // Weighted combine of the expert rows back into token order (w == nullptr:
 // unweighted sum).

@@ -229,19 +229,25 @@ moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const flo
     return from_cuda(launch_topk(s, logits, idx, w, st, zero_word), "top-k launch");
 }
 
+// a_local: x_perm is x itself, every segment the T tokens in order (k == E).
 moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offsets,
                          const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
-                         const DevStatus &ds, cudaStream_t st) {
+                         const DevStatus &ds, cudaStream_t st, bool a_local = false) {
     cudaError_t e;
     if (s.bf16)
-        e = launch_grouped_swiglu_tc(s, x_perm, offsets, Wgu, Wd, h_perm, y_perm, ds, st);
+        e = launch_grouped_swiglu_tc(s, x_perm, offsets, Wgu, Wd, h_perm, y_perm, ds, st, a_local);
     else
         e = launch_grouped_swiglu_f32(s, static_cast<const float *>(x_perm), offsets,
                                       static_cast<const float *>(Wgu),
                                       static_cast<const float *>(Wd), static_cast<float *>(h_perm),
-                                      static_cast<float *>(y_perm), st);
+                                      static_cast<float *>(y_perm), st, a_local);
     return from_cuda(e, "grouped SwiGLU launch");
 }
+
+// k == E with the weights on the outputs: every expert receives every token
+// unscaled, so moe_forward skips the permutation of x (see
+// launch_dispatch_all_experts) and the experts read x directly.
+bool all_experts_path(const Shape &s) { return s.k == s.E && !s.scale_inputs; }
 
 }  // namespace
 }  // namespace moe
@@ -317,7 +323,8 @@ int moe_forward_kernel_launches(const moe_config_t *cfg) {
     // CUDA cores selecting in the logits launch, or CUDA-core logits + top-k
     const int route = router_tc_eligible(s) ? 3 : router_selects_in_logits(s) ? 1 : 2;
     const int experts = s.bf16 ? grouped_swiglu_tc_launches(s) : 2 /* G1, G2 */;
-    return route + 2 /* rank (with the count scan), place rows */ + experts + 1 /* combine */;
+    const int dispatch = all_experts_path(s) ? 1 : 2;  // rank (with the count scan), place rows
+    return route + dispatch + experts + 1 /* combine */;
 }
 
 void moe_set_wait_limit_ns(uint64_t ns) {
@@ -458,15 +465,21 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
          *y_perm = at<uint8_t>(ws, L.y_perm);
 
     int32_t *hist = at<int32_t>(ws, L.hist);
+    const bool all_experts = all_experts_path(s);
     // the route's last launch clears the dispatch's ticket counter
     if ((st = run_route(s, x, Wr, logit_bias, logits, idx, w, at<uint8_t>(ws, L.route), ds, cs,
-                        dispatch_ticket(s, hist))) != MOE_OK)
+                        all_experts ? nullptr : dispatch_ticket(s, hist))) != MOE_OK)
         return st;
-    if ((st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm, hist, ds, cs,
-                                        s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true),
-                        "dispatch launch")) != MOE_OK)
-        return st;
-    if ((st = run_experts(s, x_perm, offsets, W_gate_up, W_down, h_perm, y_perm, ds, cs)) != MOE_OK)
+    if (all_experts)
+        st = from_cuda(launch_dispatch_all_experts(s, idx, counts, offsets, pos, src, ds, cs),
+                       "dispatch launch");
+    else
+        st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm, hist, ds, cs,
+                                       s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true),
+                       "dispatch launch");
+    if (st != MOE_OK) return st;
+    if ((st = run_experts(s, all_experts ? x : x_perm, offsets, W_gate_up, W_down, h_perm, y_perm,
+                          ds, cs, all_experts)) != MOE_OK)
         return st;
     return from_cuda(launch_combine(s, y_perm, pos, s.scale_inputs ? nullptr : w, out, cs),
                      "combine launch");

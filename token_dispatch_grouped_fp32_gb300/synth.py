@@ -16,11 +16,16 @@ gptoss_decode      64     2880  128  4   2880   bf16   gpt-oss-120b, decode
 gptoss_prefill     8192   2880  128  4   2880   bf16   gpt-oss-120b, prefill
 qwen3_zipf         16384  2048  128  8   768    bf16   Zipf-skewed routing
 deepseek           8192   7168  256  8   2048   bf16   DeepSeek-V3 routed experts
+mixtral_norenorm   4096   4096  8    2   14336  bf16   top-k weights kept as
+                                                       softmax probabilities
+mixtral_dense      1024   4096  8    8   14336  bf16   k = E: the dense soft
+                                                       mixture of all experts
 =================  =====  ====  ===  ==  =====  =====  ======================
 
 The router weight is always fp32 (E x d, nn.Linear layout).  The packed
 gate/up weight is E x d x 2f (gate in the first f columns) and the down weight
-E x f x d, both in the activation dtype.  Renormalised top-k weights throughout.
+E x f x d, both in the activation dtype.  Renormalised top-k weights except in
+the two workloads that say otherwise.
 
 Skewed routing (qwen3_zipf): a seeded random permutation gives each expert a
 rank r in 1..E, and a per-expert logit offset 3 * r**-1.2 is added to the
@@ -72,6 +77,8 @@ WORKLOADS = {
         Workload("gptoss_prefill", 8192, 2880, 128, 4, 2880, "bf16", 3),
         Workload("qwen3_zipf", 16384, 2048, 128, 8, 768, "bf16", 4, zipf=True),
         Workload("deepseek", 8192, 7168, 256, 8, 2048, "bf16", 5),
+        Workload("mixtral_norenorm", 4096, 4096, 8, 2, 14336, "bf16", 6, renorm=False),
+        Workload("mixtral_dense", 1024, 4096, 8, 8, 14336, "bf16", 7, renorm=False),
     ]
 }
 
