@@ -178,11 +178,13 @@ def oracle_sample_tokens_per_s(inp, w, budget_s: float, max_tokens: int):
     oracle.build()
     n = min(max_tokens, 8)
     t0 = time.perf_counter()
-    oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias,
+                       scale_inputs=w.scale_inputs)
     dt = time.perf_counter() - t0
     n = int(max(1, min(max_tokens, n * budget_s / max(dt, 1e-6))))
     t0 = time.perf_counter()
-    oracle.moe_forward(np.ascontiguousarray(x[:n]), Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    oracle.moe_forward(np.ascontiguousarray(x[:n]), Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias,
+                       scale_inputs=w.scale_inputs)
     dt = time.perf_counter() - t0
     return n / dt, n, dt, oracle.num_threads()
 
@@ -212,17 +214,20 @@ def run_reference(args, w):
         step_s = min(4.0, max(0.25, 120.0 / max(1, args.steps)))
     n = min(w.T, 4)
     t0 = time.perf_counter()
-    oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+    oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias,
+                       scale_inputs=w.scale_inputs)
     dt = time.perf_counter() - t0
     n = int(max(1, min(w.T, n * step_s / max(dt, 1e-6))))
     for _ in range(args.warmup if args.ref_warmup else 0):
-        oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+        oracle.moe_forward(x[:n], Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias,
+                       scale_inputs=w.scale_inputs)
     times = []
     for s in range(args.steps):
         lo = (s * n) % max(1, w.T - n + 1)
         xs = x[lo:lo + n]
         t0 = time.perf_counter()
-        oracle.moe_forward(xs, Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias)
+        oracle.moe_forward(xs, Wr, Wgu, Wd, w.k, renorm=w.renorm, bias=bias,
+                       scale_inputs=w.scale_inputs)
         times.append(time.perf_counter() - t0)
     value = n * len(times) / sum(times)
     threads = oracle.num_threads()
@@ -242,8 +247,10 @@ def run_reference(args, w):
 
 
 def workload_config(w):
-    return {"workload": f"{w.name}: T={w.T} d={w.d} E={w.E} k={w.k} f={w.f} {w.dtype}, "
-                        f"renormalised top-k{', Zipf-skewed routing' if w.zipf else ''}",
+    weights = "renormalised top-k weights" if w.renorm else "top-k softmax weights (not renormalised)"
+    return {"workload": f"{w.name}: T={w.T} d={w.d} E={w.E} k={w.k} f={w.f} {w.dtype}, {weights}"
+                        f"{', Zipf-skewed routing' if w.zipf else ''}"
+                        f"{', routing weights on the expert inputs' if w.scale_inputs else ''}",
             "T": w.T, "d": w.d, "E": w.E, "k": w.k, "f": w.f, "seed": w.seed,
             "l2": "256 MiB L2 flush between timed steps (per-step working set "
                   "also exceeds L2)"}
@@ -297,7 +304,7 @@ def measure_workload(moe, w, args, dev, rank, world, flush, with_e2e):
     inp = synth.make_inputs(wr, device=dev)
     x, Wr, Wgu, Wd = inp["x"], inp["Wr"], inp["Wgu"], inp["Wd"]
     bias = inp["bias"]
-    layer = moe.MoELayer(Wr, Wgu, Wd, w.k, bias, w.renorm)
+    layer = moe.MoELayer(Wr, Wgu, Wd, w.k, bias, w.renorm, w.scale_inputs)
     T = w.T
     cfg = layer.config(T)
     ws = layer.workspace(T)
@@ -363,7 +370,7 @@ def measure_workload(moe, w, args, dev, rank, world, flush, with_e2e):
         if ev: ev[2].record(stream)
         moe.moe_grouped_swiglu(cfg, x_perm, offsets, Wgu, Wd, h_perm, y_perm, stream=stream)
         if ev: ev[3].record(stream)
-        moe.moe_combine(cfg, y_perm, pos, wt, out2, stream=stream)
+        moe.moe_combine(cfg, y_perm, pos, None if w.scale_inputs else wt, out2, stream=stream)
         if ev: ev[4].record(stream)
 
     for _ in range(args.warmup):
@@ -540,7 +547,7 @@ def run_ours(args, w):
 
     # the other workloads, each timed the same way (no e2e, no CPU baseline):
     # parity-test configurations that the headline line does not cover
-    if not args.no_all_workloads and args.tokens is None:
+    if not args.no_all_workloads and args.tokens is None and not args.scale_inputs:
         extra = {}
         for name in ALL_WORKLOADS:
             if name == w.name:
@@ -585,6 +592,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixtral")
     ap.add_argument("--tokens", type=int, default=None, help="override T")
+    ap.add_argument("--scale-inputs", action="store_true",
+                    help="routing weights on the expert inputs (the dispatch scales the rows; "
+                         "the combine sums unweighted)")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all-workloads", action="store_true",
@@ -600,6 +610,8 @@ def main(argv=None):
     w = synth.WORKLOADS[args.workload]
     if args.tokens:
         w = w.with_tokens(args.tokens)
+    if args.scale_inputs:
+        w = w.with_(scale_inputs=True)
     if args.impl == "reference":
         run_reference(args, w)
     else:

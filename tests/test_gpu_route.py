@@ -114,6 +114,43 @@ TC_SHAPES = [
 ]
 
 
+# CUDA-core logit shapes outside the tensor-core router: fp32 x with E > 32
+# (tiled FFMA kernel for T >= 2048, 32-expert groups below), bf16 x with
+# E > 256 or E not a multiple of 8, and E <= 32 with the selection in the
+# logits launch.
+SIMT_SHAPES = [
+    # T, d, E, k, dtype
+    (2048, 256, 64, 6, "f32"),     # tiled kernel, 64 x 64 blocks
+    (3000, 192, 128, 8, "f32"),    # tiled kernel, 64 x 128 blocks, ragged row tile
+    (2500, 128, 40, 4, "bf16"),    # E % 8 != 0: tiled kernel
+    (2048, 64, 520, 8, "bf16"),    # E > 256: tiled kernel, ragged column tile
+    (1000, 320, 100, 5, "f32"),    # T < 2048: 32-expert groups, top-k launch
+    (777, 96, 24, 3, "f32"),       # E <= 32: selection in the logits launch
+]
+
+
+@pytest.mark.parametrize("T,d,E,k,dtype", SIMT_SHAPES)
+def test_route_cuda_core_shapes(moe, oracle, T, d, E, k, dtype):
+    w = synth.Workload("simt_shape", T, d, E, k, 8, dtype, 57 + E)
+    inp = synth.make_inputs(w, weights=False)
+    x, Wr = inp["x"], inp["Wr"]
+    bias = torch.linspace(-0.5, 0.5, E)
+    cfg = moe.config(T, d, E, k, 8, w.torch_dtype, True)
+    assert moe.moe_route_workspace_size(cfg) == 0  # not the tensor-core router
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    wt = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    moe.moe_route(cfg, x.cuda(), Wr.cuda(), bias.cuda(), logits, idx, wt, None)
+    torch.cuda.synchronize()
+    xs, Wrs, bs = f32(x), f32(Wr), bias.numpy()
+    ref_L = oracle.router_logits(xs, Wrs, bs)
+    assert (np.abs(logits.cpu().numpy().astype(np.float64) - ref_L)
+            <= logit_tolerance(xs, Wrs, bs)).all()
+    ref_idx, ref_w = oracle.topk(logits.cpu().numpy(), k, True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.abs(wt.cpu().numpy().astype(np.float64) - ref_w).max() <= weight_tolerance(E)
+
+
 @pytest.mark.parametrize("T,d,E,k", TC_SHAPES)
 def test_route_tensor_core_shapes(moe, oracle, T, d, E, k):
     w = synth.Workload("tc_shape", T, d, E, k, 8, "bf16", 31 + E)
