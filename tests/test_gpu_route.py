@@ -122,7 +122,7 @@ SIMT_SHAPES = [
     # T, d, E, k, dtype
     (2048, 256, 64, 6, "f32"),     # tiled kernel, 64 x 64 blocks
     (3000, 192, 128, 8, "f32"),    # tiled kernel, 64 x 128 blocks, ragged row tile
-    (2500, 128, 40, 4, "bf16"),    # E % 8 != 0: tiled kernel
+    (2500, 128, 36, 4, "bf16"),    # E % 8 != 0: tiled kernel
     (2048, 64, 520, 8, "bf16"),    # E > 256: tiled kernel, ragged column tile
     (1000, 320, 100, 5, "f32"),    # T < 2048: 32-expert groups, top-k launch
     (777, 96, 24, 3, "f32"),       # E <= 32: selection in the logits launch

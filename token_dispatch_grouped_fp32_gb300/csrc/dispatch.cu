@@ -15,9 +15,9 @@
 // them).  The last block to finish (a ticket counter) scans the matrix into
 // the first row of every (expert, chunk), which also yields counts and
 // offsets, and resets the ticket for the next call.
-// Launch 2 (place_rows_kernel), a block per group of consecutive pairs: row =
-// first row of the pair's (expert, chunk) + its rank; writes pos, src_token
-// and copies the token's row into x_perm.
+// Launch 2 (place_rows_kernel), one warp per pair: row = first row of the
+// pair's (expert, chunk) + its rank; writes pos, src_token and copies the
+// token's row into x_perm.
 // Stability: rows of one expert are in ascending pair id, hence ascending
 // token id, and no atomic decides any order.
 #include <algorithm>
@@ -177,65 +177,66 @@ rank_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB
     if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call (stream order)
 }
 
-// Launch 2: block g places the G pairs [g*G, (g+1)*G) (G divides the chunk,
-// G <= kThreads).  First one thread per pair turns its packed (expert, rank)
-// into its row -- the first row of its (expert, chunk) plus its rank --
-// writes pos[q] and src_token[row]; then the warps copy the token rows into
-// x_perm, one row at a time (16-byte vectors; with SCALE, each element times
-// the pair's weight, formed in fp32 and rounded once).
+// Launch 2: one warp per pair q.  Its row is the first row of its (expert,
+// chunk) plus its rank; lane 0 writes pos[q] and src_token[row], and the warp
+// copies the token's row into x_perm (16-byte vectors; with SCALE, each
+// element times the pair's weight, formed in fp32 and rounded once).  The
+// source row is known at once, so the first vectors of the row are loaded
+// before the row lookup (packed rank, then the base), whose latency they
+// overlap.
 template <typename TA, bool SCALE>
 __global__ void __launch_bounds__(kThreads)
 place_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist,
                   const float *__restrict__ scale, int64_t P, int k, int d, int chunk, int NB,
-                  int G, int32_t *__restrict__ pos, int32_t *__restrict__ src_token,
+                  int32_t *__restrict__ pos, int32_t *__restrict__ src_token,
                   TA *__restrict__ x_perm) {
     pdl_entry();
     constexpr int EPV = 16 / sizeof(TA);
-    __shared__ int s_row[kThreads];
-    const int64_t p0 = (int64_t)blockIdx.x * G;
-    const int n = (int)min((int64_t)G, P - p0);
-    if ((int)threadIdx.x < n) {
-        const int64_t q = p0 + threadIdx.x;
-        const int v = pos[q];  // packed by launch 1
-        int row = -1;          // dropped pair: pos stays -1
-        if (v >= 0) {
-            row = hist[(int64_t)(v >> kRankBits) * NB + (int)(q / chunk)] + (v & kRankMask);
-            pos[q] = row;
-            src_token[row] = (int32_t)(q / k);
-        }
-        s_row[threadIdx.x] = row;
-    }
-    __syncthreads();
-    if (x_perm == nullptr) return;
+    constexpr int U = 4;  // vectors per lane per round
     const int lane = threadIdx.x & 31;
-    const int nvec = d / EPV;
-    for (int i = threadIdx.x >> 5; i < n; i += kWarps) {
-        const int row = s_row[i];
-        if (row < 0) continue;
-        const int64_t q = p0 + i;
-        const uint4 *src = reinterpret_cast<const uint4 *>(x + (q / k) * d);
-        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)row * d);
-        if (SCALE) {
-            const float wq = scale[q];
-            for (int v = lane; v < nvec; v += 32) {
-                float f[EPV];
-                unpack16(ldg16(src + v), f, static_cast<const TA *>(nullptr));
+    const int64_t q = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (q >= P) return;  // warp-uniform
+    const int64_t t = q / k;
+    const int nvec = x_perm != nullptr ? d / EPV : 0;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d);
+    uint4 first[U];  // round 0 of the copy, in flight during the lookup
 #pragma unroll
-                for (int j = 0; j < EPV; ++j) f[j] *= wq;
-                stg16(dst + v, pack16(f, static_cast<const TA *>(nullptr)));
-            }
-            continue;
+    for (int u = 0; u < U; ++u)
+        if (lane + 32 * u < nvec) first[u] = ldg16(src + lane + 32 * u);
+    const int v = pos[q];  // (expert << kRankBits) | rank, from launch 1
+    if (v < 0) return;     // dropped pair: pos stays -1
+    const int row = hist[(int64_t)(v >> kRankBits) * NB + (int)(q / chunk)] + (v & kRankMask);
+    __syncwarp();  // every lane has read pos[q] before lane 0 overwrites it
+    if (lane == 0) {
+        pos[q] = row;
+        src_token[row] = (int32_t)t;
+    }
+    if (nvec == 0) return;
+    uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)row * d);
+    float wq = 1.f;
+    if (SCALE) wq = scale[q];
+    auto put = [&](int i, const uint4 &val) {
+        if (SCALE) {
+            float f[EPV];
+            unpack16(val, f, static_cast<const TA *>(nullptr));
+#pragma unroll
+            for (int j = 0; j < EPV; ++j) f[j] *= wq;
+            stg16(dst + i, pack16(f, static_cast<const TA *>(nullptr)));
+        } else {
+            stg16(dst + i, val);
         }
-        int v = lane;
-        for (; v + 96 < nvec; v += 128) {
-            const uint4 a = ldg16(src + v), b = ldg16(src + v + 32), c = ldg16(src + v + 64),
-                        dd = ldg16(src + v + 96);
-            stg16(dst + v, a);
-            stg16(dst + v + 32, b);
-            stg16(dst + v + 64, c);
-            stg16(dst + v + 96, dd);
-        }
-        for (; v < nvec; v += 32) stg16(dst + v, ldg16(src + v));
+    };
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        if (lane + 32 * u < nvec) put(lane + 32 * u, first[u]);
+    for (int i0 = 32 * U; i0 < nvec; i0 += 32 * U) {
+        uint4 buf[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i0 + lane + 32 * u < nvec) buf[u] = ldg16(src + i0 + lane + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (i0 + lane + 32 * u < nvec) put(i0 + lane + 32 * u, buf[u]);
     }
 }
 
@@ -311,14 +312,6 @@ unsigned *dispatch_ticket(const Shape &s, int32_t *scratch) {
     return reinterpret_cast<unsigned *>(scratch + (size_t)s.E * (size_t)g.blocks);
 }
 
-// Pairs per place_rows_kernel block: about P / 2048 (so ~2048 blocks), a
-// power of two from 8 to 256 that divides the chunk (a multiple of 256).
-int place_group(int64_t P) {
-    int g = 8;
-    while (g < 256 && (int64_t)g * 2048 < P) g *= 2;
-    return g;
-}
-
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
@@ -346,8 +339,7 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
     launch_pdl(rank_kernel, dim3(g.blocks), dim3(kRankThreads), sh, st, idx, P, s.E, g.chunk,
                g.blocks, staged, hist, pos, counts, offsets, ticket, ds);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    const int G = place_group(P);
-    const unsigned blocks = (unsigned)((P + G - 1) / G);
+    const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
     const int32_t *chist = hist;
     if (s.bf16) {
         using T = __nv_bfloat16;
@@ -355,20 +347,19 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
         T *xp = static_cast<T *>(x_perm);
         if (scale && x_perm)
             launch_pdl(place_rows_kernel<T, true>, dim3(blocks), dim3(kThreads), 0, st, xt, chist,
-                       scale, P, s.k, s.d, g.chunk, g.blocks, G, pos, src_token, xp);
+                       scale, P, s.k, s.d, g.chunk, g.blocks, pos, src_token, xp);
         else
             launch_pdl(place_rows_kernel<T, false>, dim3(blocks), dim3(kThreads), 0, st, xt, chist,
-                       (const float *)nullptr, P, s.k, s.d, g.chunk, g.blocks, G, pos, src_token,
-                       xp);
+                       (const float *)nullptr, P, s.k, s.d, g.chunk, g.blocks, pos, src_token, xp);
     } else {
         const float *xt = static_cast<const float *>(x);
         float *xp = static_cast<float *>(x_perm);
         if (scale && x_perm)
             launch_pdl(place_rows_kernel<float, true>, dim3(blocks), dim3(kThreads), 0, st, xt,
-                       chist, scale, P, s.k, s.d, g.chunk, g.blocks, G, pos, src_token, xp);
+                       chist, scale, P, s.k, s.d, g.chunk, g.blocks, pos, src_token, xp);
         else
             launch_pdl(place_rows_kernel<float, false>, dim3(blocks), dim3(kThreads), 0, st, xt,
-                       chist, (const float *)nullptr, P, s.k, s.d, g.chunk, g.blocks, G, pos,
+                       chist, (const float *)nullptr, P, s.k, s.d, g.chunk, g.blocks, pos,
                        src_token, xp);
     }
     return cudaGetLastError();
