@@ -92,7 +92,8 @@ const char *moe_last_error_message(void);
  * Bytes of workspace moe_forward needs for `cfg` (0 when T == 0).  The same
  * buffer also satisfies moe_route and moe_dispatch.  The workspace holds the
  * router logits and scratch, routing, dispatch arrays and the permuted
- * activations x_perm, h_perm and y_perm (see moe_workspace_layout).  The
+ * activations h_perm, y_perm and, where moe_forward uses it, x_perm (see
+ * moe_workspace_layout).  The
  * router's share depends on the current device's SM count (its K splits
  * fill one wave); with no usable device it is sized for 152 SMs.
  */
@@ -110,12 +111,17 @@ size_t moe_workspace_size(const moe_config_t *cfg);
  *   pos       int32 [P],     src_token int32 [P]   (as moe_dispatch defines them)
  *   x_perm    act [P][d],    h_perm act [P][f],    y_perm act [P][d]
  *   total     = moe_workspace_size(cfg)
- * Any other bytes of the workspace are library scratch.  With k == E and
- * the weights on the outputs (scale_inputs == 0), x_perm is not written: the
- * experts read x directly (see moe_forward).  T == 0 gives all zeros.  Returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a config
- * moe_forward would reject, or a NULL `layout`.  Launches nothing (it only
- * queries the current device's SM count, as moe_workspace_size does).
+ * Any other bytes of the workspace are library scratch.  x_perm is
+ * MOE_WS_ABSENT (no such region: the workspace is that much smaller) when
+ * moe_forward does not form the permuted rows: with k == E and the weights
+ * on the outputs the experts read x directly, and where the first grouped
+ * GEMM gathers its rows from x it reads them through src_token (see
+ * moe_forward).  T == 0 gives all zeros.  Returns MOE_ERR_INVALID_ARG /
+ * MOE_ERR_UNSUPPORTED for a config moe_forward would reject, or a NULL
+ * `layout`.  Launches nothing (it only queries the current device's SM
+ * count, as moe_workspace_size does).
  */
+#define MOE_WS_ABSENT ((size_t)-1)
 typedef struct {
     size_t logits, topk_idx, topk_w, counts, offsets, pos, src_token;
     size_t x_perm, h_perm, y_perm;
@@ -278,6 +284,12 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm,
  * [EP]: expert e's segment is rows e*T .. e*T + T-1 in token order, the
  * dispatch only writes counts, offsets, pos and src_token, and the first
  * grouped GEMM reads the rows of x itself instead of x_perm.
+ * Otherwise, for bf16 activations with the weights on the outputs, d a
+ * multiple of 64 and f <= 2048, the permuted copy of x is not formed
+ * either: the dispatch writes counts, offsets, pos and src_token, and the
+ * first grouped GEMM gathers row r of the segments from x[src_token[r]]
+ * itself (measured faster there than writing and reading x_perm; the
+ * results are bit-identical).
  * x [T][d], Wr [E][d] fp32, logit_bias [E] fp32 or NULL,
  * W_gate_up [E][d][2f], W_down [E][f][d], out [T][d] (written).
  * ws: at least moe_workspace_size(cfg) bytes, 256-byte aligned; its

@@ -106,7 +106,9 @@ def test_route_workspace_size(moe):
     cfg = moe.config(T, d, E, 8, 2048, "bf16")
     st = moe.moe_route(cfg, 16, 16, None, 16, 16, 16, 16, n - 1, stream=0, raise_on_error=False)
     assert st == moe.MOE_ERR_WORKSPACE
-    assert moe.moe_workspace_size(cfg) >= n + 2 * T * 8 * (d + 2048 + d)
+    # moe_forward's workspace also holds h_perm and y_perm (this shape gathers
+    # its rows through src_token, so it holds no x_perm)
+    assert moe.moe_workspace_size(cfg) >= n + 2 * T * 8 * (2048 + d)
 
 
 def test_workspace_too_small(moe):
@@ -186,19 +188,31 @@ def test_wait_limit_has_a_floor_outside_the_test_hook(moe):
     assert moe.moe_wait_limit_ns() == 2_000_000_000
 
 
-@pytest.mark.parametrize("T,d,E,k,f,dtype", [(4096, 4096, 8, 2, 14336, "bf16"),
-                                             (8192, 7168, 256, 8, 2048, "bf16"),
-                                             (64, 128, 8, 2, 256, "f32"), (1, 64, 3, 3, 8, "bf16")])
-def test_workspace_layout(moe, T, d, E, k, f, dtype):
+@pytest.mark.parametrize("T,d,E,k,f,dtype,scale,x_perm", [
+    (4096, 4096, 8, 2, 14336, "bf16", False, True),   # f > 2048: the permuted copy
+    (8192, 7168, 256, 8, 2048, "bf16", False, False),  # gathered rows
+    (8192, 7168, 256, 8, 2048, "bf16", True, True),    # weights on the inputs: scaled copy
+    (8192, 7200, 256, 8, 2048, "bf16", False, True),   # d not a multiple of 64
+    (64, 128, 8, 2, 256, "f32", False, True),          # fp32 path
+    (1, 64, 3, 3, 8, "bf16", False, False),           # k == E: x itself
+    (1, 64, 3, 3, 8, "bf16", True, True)])
+def test_workspace_layout(moe, T, d, E, k, f, dtype, scale, x_perm):
     """The documented regions of moe_forward's workspace are 256-byte
-    aligned, in order, large enough for their arrays, and inside the total."""
-    cfg = moe.config(T, d, E, k, f, dtype)
+    aligned, in order, large enough for their arrays, and inside the total;
+    x_perm is absent exactly where moe_forward forms no permuted copy of x
+    (k == E with the weights on the outputs, or the gathered-row path: bf16,
+    weights on the outputs, d a multiple of 64, f <= 2048), and the total
+    is then that much smaller."""
+    cfg = moe.config(T, d, E, k, f, dtype, scale_inputs=scale)
     L = moe.moe_workspace_layout(cfg)
     es = 2 if dtype == "bf16" else 4
     P = T * k
     regions = [("logits", 4 * T * E), ("topk_idx", 4 * P), ("topk_w", 4 * P), ("counts", 4 * E),
                ("offsets", 4 * (E + 1)), ("pos", 4 * P), ("src_token", 4 * P),
-               ("x_perm", es * P * d), ("h_perm", es * P * f), ("y_perm", es * P * d)]
+               ("h_perm", es * P * f), ("y_perm", es * P * d)]
+    assert (L.x_perm != moe.MOE_WS_ABSENT) == x_perm
+    if x_perm:
+        regions.append(("x_perm", es * P * d))
     spans = sorted((getattr(L, n), getattr(L, n) + size, n) for n, size in regions)
     for (a0, a1, n), (b0, _, m) in zip(spans, spans[1:]):
         assert a1 <= b0, (n, m)  # no overlap

@@ -10,7 +10,9 @@ workspace (moe_workspace_layout) and checked:
   same expert ids bit for bit, and weights within the fp32 bound; the logits
   themselves within the fp32 summation bound of the oracle's;
 - dispatch: the oracle's counts, offsets, pos and src_token for those ids,
-  bit for bit; every x_perm row a byte copy of its token's row;
+  bit for bit; every x_perm row a byte copy of its token's row (where
+  moe_forward forms x_perm; where its first grouped GEMM gathers the rows
+  through src_token, the expert checks below cover the gather);
 - experts: for EVERY expert that received rows, its first row, its last row
   (in the ragged last row tile) and the rows on each side of its tile
   boundaries, h_perm and y_perm against the oracle's FFN of that token's row,
@@ -67,7 +69,10 @@ def run(moe, request):
         "offsets": _region(ws, L.offsets, w.E + 1, torch.int32),
         "pos": _region(ws, L.pos, P, torch.int32),
         "src": _region(ws, L.src_token, P, torch.int32),
-        "x_perm": _region(ws, L.x_perm, P * w.d, dt).view(P, w.d),
+        # absent where moe_forward forms no permuted copy of x (k == E, or
+        # the first grouped GEMM gathers its rows through src_token)
+        "x_perm": (None if L.x_perm == moe.MOE_WS_ABSENT
+                   else _region(ws, L.x_perm, P * w.d, dt).view(P, w.d)),
         "h_perm": _region(ws, L.h_perm, P * w.f, dt).view(P, w.f),
         "y_perm": _region(ws, L.y_perm, P * w.d, dt).view(P, w.d),
     }
@@ -105,7 +110,8 @@ def test_full_size_routing_and_dispatch(oracle, run):
     # read x itself, and each segment holds the tokens in order)
     if w.k == w.E:
         np.testing.assert_array_equal(rs, np.tile(np.arange(w.T), w.E))
-    else:
+        assert r["x_perm"] is None
+    elif r["x_perm"] is not None:
         src = torch.from_numpy(rs).long().cuda()
         assert torch.equal(r["x_perm"], r["inp"]["x"][src])
 

@@ -44,6 +44,14 @@
 // is persistent (as many CTAs or pairs as fit at once) and strides over the
 // tile list.
 //
+// Rows gathered in G1 (Params::gather, the GATHER instantiation): moe_forward
+// can skip the permuted copy of x.  Two more warps then copy each stage's A
+// rows from the token rows through src_token with 16-byte cp.async into the
+// same swizzled layout (the TMA loads only B), and a third reports each
+// stage once its rows have landed (an mbarrier that tracks the copies, a
+// proxy fence, then an arrival or, in a pair, a 16-byte async copy into the
+// leader whose bytes complete the stage's full barrier).
+//
 // Roles (192 threads per CTA): one thread of warp 0 issues the TMA loads,
 // warp 1 owns the tensor memory and one of its threads issues the MMAs and
 // their commits (in a pair: the leader only, commits multicast to both CTAs,
@@ -74,7 +82,15 @@ constexpr int UMMA_K = 16;       // K per tcgen05.mma for 16-bit operands
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
 constexpr int B_ATOM_BYTES = BK * 128;        // 64 K-rows x 64 columns (128 B) = 8 KB
 constexpr int TMEM_COLS = 2 * BN;             // two accumulators
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;  // launches whose A operand arrives by TMA
+// G1 launches that gather their A rows from the token rows (Params::gather)
+// add kGatherWarps warps, which copy the rows of every A stage, and one warp
+// that reports each stage to the MMA issuer once its rows have landed.  Two
+// copying warps measured faster than one or four.
+constexpr int kGatherWarps = 2;
+constexpr int NUM_THREADS_GATHER = NUM_THREADS + 32 * (kGatherWarps + 1);
+constexpr int kGatherRows = 128 / kGatherWarps;  // A rows per gather warp and stage
+constexpr int kGatherIters = kGatherRows / 4;    // a warp instruction copies 4 rows
 constexpr int MAX_E = 1024;
 constexpr int kPairRowsPerExpert = 512;  // average rows per expert that selects CTA pairs
 
@@ -90,8 +106,12 @@ template <int CTAS> struct Cfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = STAGES * A_BYTES;
     static constexpr int OFF_BAR = OFF_B + STAGES * B_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;  // full, empty, tmem full/empty, drain
-    static constexpr int OFF_TMEM = OFF_BAR + NUM_BARS * 8;
+    // full, empty, tmem full/empty, drain, gathered (rows copied, per stage)
+    static constexpr int NUM_BARS = 3 * STAGES + 2 + 2 + 1;
+    // gathered stages of a pair are reported by 16-byte copies into the
+    // leader's shared memory (one slot per CTA)
+    static constexpr int OFF_SIGNAL = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;
+    static constexpr int OFF_TMEM = OFF_SIGNAL + 16 * CTAS;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_OFFS = OFF_ABORT + 4;               // int[MAX_E + 1]
     static constexpr int OFF_TILE = OFF_OFFS + 4 * (MAX_E + 1);  // int[MAX_E + 1]
@@ -129,6 +149,13 @@ struct Params {
     // G1's A holds one row per position of a segment: row r of expert e
     // reads A row r - offsets[e] (every expert sees every token, in order)
     int a_local;
+    // G1's A rows are gathered from the token rows: row r of the segments is
+    // row src_token[r] of gx ([T][K], K a multiple of 64), copied by the
+    // gather warps; no permuted copy of the activations exists.  The launch
+    // runs the GATHER instantiation of the kernel.
+    int gather;
+    const __nv_bfloat16 *gx;
+    const int32_t *src_token;
     DevStatus ds;
 };
 
@@ -228,8 +255,8 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *s_off, cons
 }
 
 // tmX / tmWgu: A and B of G1; tmH / tmWd: A and B of G2.
-template <int CTAS>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int CTAS, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmWgu,
                        const __grid_constant__ CUtensorMap tmH,
@@ -248,6 +275,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     const uint32_t bar_tfull = bar_empty + 8 * STAGES;     // [2]
     const uint32_t bar_tempty = bar_tfull + 16;            // [2] (a pair uses the leader's)
     const uint32_t bar_drain = bar_tempty + 16;
+    const uint32_t bar_gat = bar_drain + 8;                // [STAGES] (p.gather)
     volatile uint32_t *s_tmem = reinterpret_cast<volatile uint32_t *>(base + C::OFF_TMEM);
     volatile int *s_abort = reinterpret_cast<volatile int *>(base + C::OFF_ABORT);
     int *s_off = reinterpret_cast<int *>(base + C::OFF_OFFS);
@@ -267,9 +295,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     // kernel has completed) the row-tile prefix from `offsets` ----
     if (threadIdx.x == 0) {
         *s_abort = 0;
+        // a stage is full when the leader's producer has armed it and its
+        // bytes have landed; with GATHER, also once the reporting warp of
+        // each CTA has seen its gathered rows land (bar_gat: one arrival per
+        // gather thread) and reported them: a single CTA arrives, a pair
+        // sends 16 bytes per CTA that count as transaction bytes
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_full + 8 * i, GATHER && !PAIR ? 2 : 1);
             mbar_init(bar_empty + 8 * i, 1);
+            mbar_init(bar_gat + 8 * i, 32 * kGatherWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_tfull + 8 * i, 1);
@@ -283,7 +317,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
     if (!p.overlap_prev) pdl_wait();
     if (p.release_late) pdl_release();
     // through L2: with overlap_prev no grid-wide wait precedes this read
-    for (int e = threadIdx.x; e <= E; e += NUM_THREADS) s_off[e] = __ldcg(p.offsets + e);
+    for (int e = threadIdx.x; e <= E; e += (int)blockDim.x) s_off[e] = __ldcg(p.offsets + e);
     __syncthreads();
     if (warp == 2) {  // prefix over experts of their row tiles in this launch
         const int per = (E + 31) / 32;
@@ -344,12 +378,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     }
                     const uint32_t fb = sig_full + 8 * s;
                     const int k0 = ks * BK;
+                    const bool a_tma = !(GATHER && !ti.down);  // else the gather warps fill A
                     if (leader) {
-                        mbar_arrive_expect_tx(bar_full + 8 * s, C::EXPECT_BYTES);
+                        mbar_arrive_expect_tx(bar_full + 8 * s,
+                                              a_tma ? C::EXPECT_BYTES
+                                                    : (C::B_BYTES + (PAIR ? 16 : 0)) * CTAS);
                         issued |= 1u << s;
                         last_par = (last_par & ~(1u << s)) | (ph << s);
                     }
-                    tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, tmA, k0, arow, fb);
+                    if (a_tma) tma_load_2d<CTAS>(base_s + C::OFF_A + s * A_BYTES, tmA, k0, arow, fb);
                     const uint32_t bdst = base_s + C::OFF_B + s * C::B_BYTES;
                     if (p.b_blocks) {
                         // two atoms per box (weights viewed by 64-column blocks)
@@ -414,7 +451,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int ks = 0; ks < nk; ++ks) {
-                    if (!wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort)) {
+                    // gathered A of a pair: the peer's rows are reported by
+                    // its warps' cluster-scope arrivals
+                    const bool full = PAIR && GATHER
+                                          ? wait_bounded<true>(bar_full + 8 * s, ph, p.ds, s_abort)
+                                          : wait_bounded(bar_full + 8 * s, ph, p.ds, s_abort);
+                    if (!full) {
                         ok = false;
                         break;
                     }
@@ -441,7 +483,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
             wait_bounded(bar_drain, 0, p.ds, &never, drain_limit(p.ds));
         }
         __syncwarp();
-    } else {
+    } else if (warp < 6) {
         // --------------------------- epilogue ----------------------------
         const int quarter = warp & 3;  // tensor-memory lanes [32*quarter, 32*quarter + 32)
         const int r_in_tile = (int)rank * BM + quarter * 32 + lane;
@@ -563,6 +605,87 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                 else mbar_arrive(bar_tempty + 8 * acc);
             }
         }
+    } else if (GATHER && warp < 6 + kGatherWarps) {
+        // --------------------- G1 A rows gathered (GATHER) ---------------------
+        // Gather warp g fills rows [Rg, Rg + R) of this CTA's 128 A rows
+        // (R = kGatherRows) in every stage: lane (j8 = lane / 8, c = lane % 8)
+        // copies 16-byte chunk c of rows Rg + 4i + j8, each the K step's 64
+        // columns of token row src_token[row], to where the TMA would put it
+        // (row * 128 bytes, chunk c at (c ^ (row % 8)) * 16: the 128-byte
+        // swizzle).  Rows past the tile's end are not copied; their
+        // accumulator rows are never stored.  Every thread then has the
+        // stage's bar_gat receive its arrival once its copies have landed,
+        // and moves on: up to STAGES stages of copies are in flight.
+        const int g = warp - 6;
+        const int j8 = lane >> 3, c = lane & 7;
+        const int K = p.g1.K;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int tile = unit; tile < total && ok; tile += nunits) {
+            const TileInfo ti = decode_tile(tile, s_off, s_tile, E, total1, n1, n2, C::TILE_M);
+            int64_t off[kGatherIters];  // element offset of this lane's chunk; -1: past the tile
+#pragma unroll
+            for (int i = 0; i < kGatherIters; ++i) {
+                const int lr = kGatherRows * g + 4 * i + j8;  // row within this CTA's 128
+                const int rt = (int)rank * BM + lr;           // row within the tile
+                off[i] = rt < ti.rows ? (int64_t)__ldcg(p.src_token + ti.row0 + rt) * K + 8 * c : -1;
+            }
+            for (int ks = 0; ks < nk1; ++ks) {
+                if (!__all_sync(0xffffffffu, wait_bounded(bar_empty + 8 * s, ph ^ 1u, p.ds, s_abort))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = base_s + C::OFF_A + s * A_BYTES;
+#pragma unroll
+                for (int i = 0; i < kGatherIters; ++i) {
+                    const int lr = kGatherRows * g + 4 * i + j8;
+                    if (off[i] >= 0)
+                        cp_async16(dst + lr * 128 + ((c ^ (lr & 7)) << 4), p.gx + off[i] + ks * BK);
+                }
+                cp_async_mbar_arrive_noinc(bar_gat + 8 * s);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        cp_async_wait_all();  // every copy lands before the shared memory is released
+    } else if (GATHER) {
+        // --------------- G1 gathered stages reported (GATHER) ----------------
+        // Once a stage's gathered rows have landed (bar_gat), one thread
+        // orders them before the tensor cores' reads (proxy fence) and
+        // reports the stage on its full barrier: a single CTA arrives on its
+        // own; a CTA of a pair copies 16 bytes of the stage into its slot in
+        // the leader's shared memory, an async-proxy copy ordered after the
+        // fence, whose completion counts as transaction bytes on the
+        // leader's full barrier (an arrival with release at cluster scope,
+        // once per stage, measured about twice as slow).
+        const uint32_t slot = PAIR ? map_to_rank(base_s + C::OFF_SIGNAL + 16 * rank, 0) : 0u;
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int tile = unit; tile < total && ok; tile += nunits) {
+                for (int ks = 0; ks < nk1; ++ks) {
+                    if (!wait_bounded(bar_gat + 8 * s, ph, p.ds, s_abort)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_smem();
+                    if (PAIR)
+                        bulk_copy_to_cluster(slot, base_s + C::OFF_A + s * A_BYTES, 16,
+                                             sig_full + 8 * s);
+                    else
+                        mbar_arrive(bar_full + 8 * s);
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+        }
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -581,10 +704,11 @@ struct DeviceInfo {
 };
 
 template <int CTAS>
-cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttribute *attr) {
+cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttribute *attr,
+                                 int threads) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = Cfg<CTAS>::SMEM_BYTES;
     cfg.stream = st;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -603,18 +727,35 @@ cudaError_t launch(unsigned grid, const CUtensorMap &mx, const CUtensorMap &mwgu
                    const CUtensorMap &mh, const CUtensorMap &mwd, const Params &p,
                    cudaStream_t st) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<CTAS>(grid, st, attr);
-    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS>, mx, mwgu, mh, mwd, p);
+    cudaLaunchConfig_t cfg =
+        launch_config<CTAS>(grid, st, attr, p.gather ? NUM_THREADS_GATHER : NUM_THREADS);
+    return p.gather ? cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS, true>, mx, mwgu, mh, mwd, p)
+                    : cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS, false>, mx, mwgu, mh, mwd, p);
 }
 
+// Both instantiations fit one CTA per SM (shared memory); the resident
+// count is the smaller of the two.
 template <int CTAS> cudaError_t prepare(int *resident_units) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Cfg<CTAS>::SMEM_BYTES);
-    if (err != cudaSuccess) return err;
+    cudaError_t err;
+    if ((err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg<CTAS>::SMEM_BYTES)) != cudaSuccess ||
+        (err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg<CTAS>::SMEM_BYTES)) != cudaSuccess)
+        return err;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<CTAS>(CTAS, nullptr, attr);
-    return cudaOccupancyMaxActiveClusters(resident_units, grouped_gemm_tc_kernel<CTAS>, &cfg);
+    int a = 0, b = 0;
+    cudaLaunchConfig_t cfg = launch_config<CTAS>(CTAS, nullptr, attr, NUM_THREADS);
+    if ((err = cudaOccupancyMaxActiveClusters(&a, grouped_gemm_tc_kernel<CTAS, false>, &cfg)) !=
+        cudaSuccess)
+        return err;
+    cfg = launch_config<CTAS>(CTAS, nullptr, attr, NUM_THREADS_GATHER);
+    if ((err = cudaOccupancyMaxActiveClusters(&b, grouped_gemm_tc_kernel<CTAS, true>, &cfg)) !=
+        cudaSuccess)
+        return err;
+    *resident_units = std::min(a, b);
+    return cudaSuccess;
 }
 
 // Upper bound of the row tiles: sum_e ceil(count_e/TM) <= P/TM + min(E, P).
@@ -647,6 +788,7 @@ cudaError_t launch_product(const Shape &s, int units, const CUtensorMap &mx,
     p.experts = experts;
     if (phase == 1) p.g2.n_tiles = 0;
     else p.g1.n_tiles = 0;
+    if (phase == 2) p.gather = 0;  // G2's A (h_perm) is read by TMA
     const int64_t n_tiles = phase == 1 ? both.g1.n_tiles : both.g2.n_tiles;
     const unsigned grid = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles);
     return launch<CTAS>(grid, mx, mwgu, mh, mwd, p, st);
@@ -672,9 +814,25 @@ int grouped_swiglu_tc_launches(const Shape &s) {
     return tc::tile_mode(s) == tc::kModeHybrid ? 4 : 2;
 }
 
+// The row gather needs whole 64-column K steps.
+bool grouped_swiglu_tc_gathers(const Shape &s) { return s.d % tc::BK == 0; }
+
+// Gathering G1's rows saves the permuted copy of x (written once, read once)
+// and costs the gather kernel's throughput (its extra warps hold the block's
+// registers to 168 a thread, and its copies share the SM's intake with the
+// weight tiles).  The saving per FLOP falls as 1/f; measured against the
+// copying path, the layer ran 3-6 % faster at f = 768 (Qwen3-30B-A3B
+// shape), 1.4 % at f = 2048 (DeepSeek-V3 shape), no faster at f = 2880
+// (gpt-oss) and 3 % slower at f = 14336 (Mixtral shape).
+constexpr int kGatherMaxF = 2048;
+bool grouped_swiglu_tc_gather_pays(const Shape &s) {
+    return grouped_swiglu_tc_gathers(s) && s.f <= kGatherMaxF;
+}
+
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
-                                     const DevStatus &ds, cudaStream_t st, bool a_local) {
+                                     const DevStatus &ds, cudaStream_t st, bool a_local,
+                                     const int32_t *src_token) {
     using namespace tc;
     static DeviceInfo info[64];
     int dev = 0;
@@ -707,8 +865,15 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
                      tensor_map_weight_blocks(&mwd, Wd, s.E, s.f, s.d, 2)
                : tensor_map_weights(&mwgu, Wgu, s.E, s.d, 2 * (int64_t)s.f) &&
                      tensor_map_weights(&mwd, Wd, s.E, s.f, s.d);
+    // gather (src_token given): x_perm is the T token rows, G1's A rows are
+    // gathered from them; d must be whole 64-column K steps
+    const bool gather = src_token != nullptr;
+    if (gather && (a_local || !grouped_swiglu_tc_gathers(s))) {
+        set_error_message("the row gather needs d a multiple of %d and no local rows", BK);
+        return cudaErrorInvalidValue;
+    }
     // a_local: G1's A is the T token rows themselves
-    if (!maps_ok || !tensor_map_rows(&mx, x_perm, a_local ? s.T : P, s.d, BM) ||
+    if (!maps_ok || !tensor_map_rows(&mx, x_perm, a_local || gather ? s.T : P, s.d, BM) ||
         !tensor_map_rows(&mh, h_perm, P, s.f, BM)) {
         set_error_message("cuTensorMapEncodeTiled rejected an operand (alignment or size)");
         return cudaErrorInvalidValue;
@@ -737,6 +902,9 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     p.overlap_prev = 0;
     p.b_blocks = blocks ? 1 : 0;
     p.a_local = a_local ? 1 : 0;
+    p.gather = gather ? 1 : 0;
+    p.gx = static_cast<const __nv_bfloat16 *>(x_perm);
+    p.src_token = src_token;
     p.ds = ds;
     // G1 launches, then G2 launches (G2 reads h_perm; stream order)
     const TileMode mode = tile_mode(s);

@@ -74,11 +74,18 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
 // Kernel launches of one launch_grouped_swiglu_tc call (2, or 4 when the
 // experts are split between CTA-pair and single-CTA tiles).
 int grouped_swiglu_tc_launches(const Shape &s);
+// Whether launch_grouped_swiglu_tc can gather G1's rows (src_token) for s,
+// and whether doing so is measured faster than reading a permuted copy.
+bool grouped_swiglu_tc_gathers(const Shape &s);
+bool grouped_swiglu_tc_gather_pays(const Shape &s);
 // a_local: x_perm is the T token rows x, and row r of expert e's segment
 // reads row r - offsets[e] (every expert receives every token, in order).
+// src_token (not null): x_perm is the T token rows x, and G1 gathers row r
+// of the segments from row src_token[r] (d a multiple of 64, no a_local).
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
-                                     const DevStatus &ds, cudaStream_t st, bool a_local = false);
+                                     const DevStatus &ds, cudaStream_t st, bool a_local = false,
+                                     const int32_t *src_token = nullptr);
 cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const int32_t *offsets,
                                       const float *Wgu, const float *Wd, float *h_perm,
                                       float *y_perm, cudaStream_t st, bool a_local = false);

@@ -171,6 +171,22 @@ moe_status_t from_cuda(cudaError_t e, const char *what) {
     return MOE_ERR_CUDA;
 }
 
+// k == E with the weights on the outputs: every expert receives every token
+// unscaled, so moe_forward skips the permutation of x (see
+// launch_dispatch_all_experts) and the experts read x directly.
+bool all_experts_path(const Shape &s) { return s.k == s.E && !s.scale_inputs; }
+
+// bf16 with the weights on the outputs, where the grouped GEMM's row gather
+// pays (grouped_swiglu_tc_gather_pays): the dispatch only ranks and places
+// the pairs, and the first expert GEMM gathers its rows from x through
+// src_token.
+bool gather_path(const Shape &s) {
+    return s.bf16 && !s.scale_inputs && !all_experts_path(s) && grouped_swiglu_tc_gather_pays(s);
+}
+
+// moe_forward writes and reads x_perm unless its experts read x itself.
+bool forward_uses_x_perm(const Shape &s) { return !all_experts_path(s) && !gather_path(s); }
+
 // ----- workspace layout of moe_forward (256-byte aligned sub-buffers) -----
 struct WsLayout {
     size_t logits, idx, w, counts, offsets, pos, src, hist, route, x_perm, h_perm, y_perm, total;
@@ -191,7 +207,12 @@ WsLayout ws_layout(const Shape &s) {
     L.src = o;    o = up256(o + 4 * P);
     L.hist = o;   o = up256(o + dispatch_scratch_bytes(s));
     L.route = o;  o = up256(o + router_tc_scratch_bytes(s));
-    L.x_perm = o; o = up256(o + es * P * s.d);
+    if (forward_uses_x_perm(s)) {
+        L.x_perm = o;
+        o = up256(o + es * P * s.d);
+    } else {
+        L.x_perm = MOE_WS_ABSENT;
+    }
     L.h_perm = o; o = up256(o + es * P * s.f);
     L.y_perm = o; o = up256(o + es * P * s.d);
     L.total = o;
@@ -230,12 +251,15 @@ moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const flo
 }
 
 // a_local: x_perm is x itself, every segment the T tokens in order (k == E).
+// src_token (bf16 only): x_perm is x itself and G1 gathers its rows.
 moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offsets,
                          const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
-                         const DevStatus &ds, cudaStream_t st, bool a_local = false) {
+                         const DevStatus &ds, cudaStream_t st, bool a_local = false,
+                         const int32_t *src_token = nullptr) {
     cudaError_t e;
     if (s.bf16)
-        e = launch_grouped_swiglu_tc(s, x_perm, offsets, Wgu, Wd, h_perm, y_perm, ds, st, a_local);
+        e = launch_grouped_swiglu_tc(s, x_perm, offsets, Wgu, Wd, h_perm, y_perm, ds, st, a_local,
+                                     src_token);
     else
         e = launch_grouped_swiglu_f32(s, static_cast<const float *>(x_perm), offsets,
                                       static_cast<const float *>(Wgu),
@@ -244,10 +268,6 @@ moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offs
     return from_cuda(e, "grouped SwiGLU launch");
 }
 
-// k == E with the weights on the outputs: every expert receives every token
-// unscaled, so moe_forward skips the permutation of x (see
-// launch_dispatch_all_experts) and the experts read x directly.
-bool all_experts_path(const Shape &s) { return s.k == s.E && !s.scale_inputs; }
 
 }  // namespace
 }  // namespace moe
@@ -461,11 +481,12 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
     float *w = at<float>(ws, L.w);
     int32_t *counts = at<int32_t>(ws, L.counts), *offsets = at<int32_t>(ws, L.offsets);
     int32_t *pos = at<int32_t>(ws, L.pos), *src = at<int32_t>(ws, L.src);
-    void *x_perm = at<uint8_t>(ws, L.x_perm), *h_perm = at<uint8_t>(ws, L.h_perm),
-         *y_perm = at<uint8_t>(ws, L.y_perm);
+    void *x_perm = L.x_perm == MOE_WS_ABSENT ? nullptr : at<uint8_t>(ws, L.x_perm);
+    void *h_perm = at<uint8_t>(ws, L.h_perm), *y_perm = at<uint8_t>(ws, L.y_perm);
 
     int32_t *hist = at<int32_t>(ws, L.hist);
     const bool all_experts = all_experts_path(s);
+    const bool gather = gather_path(s);
     // the route's last launch clears the dispatch's ticket counter
     if ((st = run_route(s, x, Wr, logit_bias, logits, idx, w, at<uint8_t>(ws, L.route), ds, cs,
                         all_experts ? nullptr : dispatch_ticket(s, hist))) != MOE_OK)
@@ -474,12 +495,13 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
         st = from_cuda(launch_dispatch_all_experts(s, idx, counts, offsets, pos, src, ds, cs),
                        "dispatch launch");
     else
-        st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src, x_perm, hist, ds, cs,
+        st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src,
+                                       gather ? nullptr : x_perm, hist, ds, cs,
                                        s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true),
                        "dispatch launch");
     if (st != MOE_OK) return st;
-    if ((st = run_experts(s, all_experts ? x : x_perm, offsets, W_gate_up, W_down, h_perm, y_perm,
-                          ds, cs, all_experts)) != MOE_OK)
+    if ((st = run_experts(s, all_experts || gather ? x : x_perm, offsets, W_gate_up, W_down, h_perm,
+                          y_perm, ds, cs, all_experts, gather ? src : nullptr)) != MOE_OK)
         return st;
     return from_cuda(launch_combine(s, y_perm, pos, s.scale_inputs ? nullptr : w, out, cs),
                      "combine launch");

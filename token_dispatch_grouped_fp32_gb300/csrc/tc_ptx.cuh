@@ -33,15 +33,27 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
+// CLUSTER: acquire at cluster scope, for phases completed by arrivals (with
+// release at cluster scope) from the other CTA of a pair.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -55,6 +67,48 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                  : "memory");
+}
+// 16-byte copy global -> this CTA's shared memory through L2 (no L1
+// allocation), asynchronous to the issuing thread; groups of them are
+// committed and waited for with the two functions after it.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N> __device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Have barrier `bar` (this CTA's) receive one arrival once every cp.async
+// this thread issued before has completed; the arrival is not added to the
+// barrier's expected count (it is one of the counts the barrier was
+// initialised with).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Wait until every cp.async this thread issued has completed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+// `bytes` (a multiple of 16) from this CTA's shared memory to the shared
+// memory of a CTA of the cluster, completing as transaction bytes on a
+// barrier of that CTA (both given as cluster-window addresses); an
+// async-proxy operation, ordered after this thread's earlier proxy fence.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src,
+                                                     uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst_cluster),
+        "r"(src), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+// Order the shared-memory writes this thread has made or observed (generic
+// proxy: stores, cp.async) before later async-proxy accesses (the tensor
+// cores' operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 // TMA tile loads into this CTA's shared memory.  CTAS = 1: completion on a
 // barrier of this CTA.  CTAS = 2: on a barrier of either CTA of the pair
@@ -217,15 +271,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 
 // Bounded wait: true when the phase with `parity` has completed; false when
 // the limit ran out or another role raised the abort flag.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
                                              volatile int *abort_flag,
                                              unsigned long long limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             raise_error(ds, kErrTimeout);
@@ -234,9 +289,10 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
         }
     }
 }
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const DevStatus &ds,
                                              volatile int *abort_flag) {
-    return wait_bounded(bar, parity, ds, abort_flag, ds.wait_limit_ns);
+    return wait_bounded<CLUSTER>(bar, parity, ds, abort_flag, ds.wait_limit_ns);
 }
 // Drain waits (in-flight copies / MMAs before the CTA frees its resources)
 // never use less than 1 s, whatever limit the caller set for the main loop.

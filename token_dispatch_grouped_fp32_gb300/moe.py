@@ -42,6 +42,10 @@ class moe_config_t(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("scale_inputs", ctypes.c_int32)]
 
 
+# moe_workspace_layout: offset of a region moe_forward does not use
+MOE_WS_ABSENT = (1 << (8 * ctypes.sizeof(ctypes.c_size_t))) - 1
+
+
 class moe_workspace_layout_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets",
                                                "pos", "src_token", "x_perm", "h_perm", "y_perm",
