@@ -17,7 +17,8 @@
 // offsets, and resets the ticket for the next call.
 // Launch 2 (place_rows_kernel), one warp per pair: row = first row of the
 // pair's (expert, chunk) + its rank; writes pos, src_token and copies the
-// token's row into x_perm.
+// token's row into x_perm.  Without x_perm (the experts gather the rows),
+// place_index_kernel does the same lookup with a thread per pair.
 // Stability: rows of one expert are in ascending pair id, hence ascending
 // token id, and no atomic decides any order.
 #include <algorithm>
@@ -240,6 +241,21 @@ place_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist,
     }
 }
 
+// Launch 2 when no row moves (x_perm == nullptr: the experts gather the rows
+// themselves): a thread per pair, the same row lookup as place_rows_kernel.
+__global__ void __launch_bounds__(kThreads)
+place_index_kernel(const int32_t *__restrict__ hist, int64_t P, int k, int chunk, int NB,
+                   int32_t *__restrict__ pos, int32_t *__restrict__ src_token) {
+    pdl_entry();
+    const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (q >= P) return;
+    const int v = pos[q];  // (expert << kRankBits) | rank, from launch 1
+    if (v < 0) return;     // dropped pair: pos stays -1
+    const int row = hist[(int64_t)(v >> kRankBits) * NB + (int)(q / chunk)] + (v & kRankMask);
+    pos[q] = row;
+    src_token[row] = (int32_t)(q / k);
+}
+
 // Every token picks every expert (k == E), each once, so expert e's segment
 // is the T tokens in order: the row of pair q = (t, j) is idx[q] * T + t.
 __global__ void __launch_bounds__(kThreads)
@@ -339,6 +355,12 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
     launch_pdl(rank_kernel, dim3(g.blocks), dim3(kRankThreads), sh, st, idx, P, s.E, g.chunk,
                g.blocks, staged, hist, pos, counts, offsets, ticket, ds);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (x_perm == nullptr) {  // pos and src_token only (moe_forward's gathered-row path)
+        launch_pdl(place_index_kernel, dim3((unsigned)((P + kThreads - 1) / kThreads)),
+                   dim3(kThreads), 0, st, static_cast<const int32_t *>(hist), P, s.k, g.chunk,
+                   g.blocks, pos, src_token);
+        return cudaGetLastError();
+    }
     const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
     const int32_t *chist = hist;
     if (s.bf16) {
