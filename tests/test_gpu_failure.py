@@ -9,7 +9,10 @@ freed and the kernel returns.  The host reads the status; the context stays
 usable and the next call (hook off, default limit) is bit-identical to one
 made before.  No trap, fault or hang is involved.  Every tile mode is
 covered: CTA pairs (Mixtral-shaped, >= 512 rows per expert), single CTAs, and
-the experts split between the two (about 128 rows per expert)."""
+the experts split between the two (about 128 rows per expert); and each of
+them again on the Qwen3 shape, whose first grouped GEMM gathers its rows (its
+copying and reporting warps give up at their next wait as well, and every
+copy they issued lands before the kernel returns)."""
 import pytest
 import torch
 
@@ -25,7 +28,9 @@ def moe():
 
 
 @pytest.mark.parametrize("name,T", [("mixtral", 4096), ("gptoss_prefill", 512),
-                                    ("gptoss_prefill", 4096)])  # pairs; single CTAs; both
+                                    ("gptoss_prefill", 4096),  # pairs; single CTAs; both
+                                    ("qwen3_zipf", 8192), ("qwen3_zipf", 512),
+                                    ("qwen3_zipf", 2048)])  # the same, rows gathered
 def test_wait_timeout_is_reported_and_recoverable(moe, name, T):
     w = synth.WORKLOADS[name].with_tokens(T)
     inp = synth.make_inputs(w, device="cuda")
