@@ -113,10 +113,9 @@ size_t moe_workspace_size(const moe_config_t *cfg);
  *   total     = moe_workspace_size(cfg)
  * Any other bytes of the workspace are library scratch.  x_perm is
  * MOE_WS_ABSENT (no such region: the workspace is that much smaller) when
- * moe_forward does not form the permuted rows: with k == E and the weights
- * on the outputs the experts read x directly, and where the first grouped
- * GEMM gathers its rows from x it reads them through src_token (see
- * moe_forward).  T == 0 gives all zeros.  Returns MOE_ERR_INVALID_ARG /
+ * moe_forward does not form the permuted rows: with k == E the experts read
+ * x directly, and where the first grouped GEMM gathers its rows from x it
+ * reads them through src_token (see moe_forward).  T == 0 gives all zeros.  Returns MOE_ERR_INVALID_ARG /
  * MOE_ERR_UNSUPPORTED for a config moe_forward would reject, or a NULL
  * `layout`.  Launches nothing (it only queries the current device's SM
  * count, as moe_workspace_size does).
@@ -279,17 +278,21 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm,
 /*
  * The whole layer, one stream, no host synchronisation: moe_route,
  * moe_dispatch, moe_grouped_swiglu, moe_combine.
- * When k == E and the weights act on the outputs (scale_inputs == 0), every
- * expert receives every token unscaled, so there is nothing to permute
- * [EP]: expert e's segment is rows e*T .. e*T + T-1 in token order, the
- * dispatch only writes counts, offsets, pos and src_token, and the first
- * grouped GEMM reads the rows of x itself instead of x_perm.
- * Otherwise, for bf16 activations with the weights on the outputs, d a
- * multiple of 64 and f <= 2048, the permuted copy of x is not formed
- * either: the dispatch writes counts, offsets, pos and src_token, and the
- * first grouped GEMM gathers row r of the segments from x[src_token[r]]
- * itself (measured faster there than writing and reading x_perm; the
- * results are bit-identical).
+ * When k == E every expert receives every token, so there is nothing to
+ * permute [EP]: expert e's segment is rows e*T .. e*T + T-1 in token order,
+ * the dispatch only writes counts, offsets, pos and src_token, and the first
+ * grouped GEMM reads the rows of x itself instead of x_perm (for fp32 with
+ * the weights on the inputs, the scaled rows are copied instead).
+ * Otherwise, for bf16 activations with d a multiple of 64 and f <= 2048, the
+ * permuted copy of x is not formed either: the dispatch writes counts,
+ * offsets, pos and src_token, and the first grouped GEMM gathers row r of
+ * the segments from x[src_token[r]] itself (measured faster there than
+ * writing and reading x_perm; with the weights on the outputs the results
+ * are bit-identical to the copying path).
+ * On both paths, weights on the inputs (scale_inputs != 0, bf16) are
+ * applied by the first grouped GEMM: row r's gate and up products are
+ * multiplied by its pair's weight in fp32 before the SwiGLU, (w x) W =
+ * w (x W), where the copying path rounds w x to bf16 first.
  * x [T][d], Wr [E][d] fp32, logit_bias [E] fp32 or NULL,
  * W_gate_up [E][d][2f], W_down [E][f][d], out [T][d] (written).
  * ws: at least moe_workspace_size(cfg) bytes, 256-byte aligned; its

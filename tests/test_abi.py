@@ -160,10 +160,14 @@ def test_forward_kernel_launches(moe):
     assert moe.moe_forward_kernel_launches(moe.config(64, 128, 8, 2, 256, "f32")) == 6
     # fp32 activations, E > 32: CUDA-core logits, then the top-k kernel
     assert moe.moe_forward_kernel_launches(moe.config(4096, 128, 64, 2, 256, "f32")) == 7
-    # k = E (weights on the outputs): one dispatch launch, no permutation
+    # k = E: one dispatch launch, no permutation (bf16 with the weights on
+    # the inputs too: the first GEMM scales the rows' products); fp32 with
+    # the weights on the inputs copies scaled rows (two dispatch launches)
     assert moe.moe_forward_kernel_launches(moe.config(1024, 4096, 8, 8, 14336, "bf16", False)) == 7
     assert moe.moe_forward_kernel_launches(
-        moe.config(1024, 4096, 8, 8, 14336, "bf16", False, scale_inputs=True)) == 8
+        moe.config(1024, 4096, 8, 8, 14336, "bf16", False, scale_inputs=True)) == 7
+    assert moe.moe_forward_kernel_launches(
+        moe.config(64, 128, 8, 8, 256, "f32", False, scale_inputs=True)) == 6
     assert moe.moe_forward_kernel_launches(moe.config(0, 128, 8, 2, 256, "bf16")) == 0
     assert moe.moe_forward_kernel_launches(moe.config(4, 4096, 8, 9, 14336)) == -1
 
@@ -191,18 +195,20 @@ def test_wait_limit_has_a_floor_outside_the_test_hook(moe):
 @pytest.mark.parametrize("T,d,E,k,f,dtype,scale,x_perm", [
     (4096, 4096, 8, 2, 14336, "bf16", False, True),   # f > 2048: the permuted copy
     (8192, 7168, 256, 8, 2048, "bf16", False, False),  # gathered rows
-    (8192, 7168, 256, 8, 2048, "bf16", True, True),    # weights on the inputs: scaled copy
+    (8192, 7168, 256, 8, 2048, "bf16", True, False),   # weights on the inputs: still gathered
+    (4096, 4096, 8, 2, 14336, "bf16", True, True),     # weights on the inputs, f > 2048: scaled copy
     (8192, 7200, 256, 8, 2048, "bf16", False, True),   # d not a multiple of 64
     (64, 128, 8, 2, 256, "f32", False, True),          # fp32 path
     (1, 64, 3, 3, 8, "bf16", False, False),           # k == E: x itself
-    (1, 64, 3, 3, 8, "bf16", True, True)])
+    (1, 64, 3, 3, 8, "bf16", True, False),           # k == E, weights on the inputs: x itself
+    (64, 128, 8, 8, 256, "f32", True, True)])          # the same in fp32: scaled copy
 def test_workspace_layout(moe, T, d, E, k, f, dtype, scale, x_perm):
     """The documented regions of moe_forward's workspace are 256-byte
     aligned, in order, large enough for their arrays, and inside the total;
     x_perm is absent exactly where moe_forward forms no permuted copy of x
-    (k == E with the weights on the outputs, or the gathered-row path: bf16,
-    weights on the outputs, d a multiple of 64, f <= 2048), and the total
-    is then that much smaller."""
+    (k == E, except fp32 with the weights on the inputs; or the gathered-row
+    path: bf16, d a multiple of 64, f <= 2048), and the total is then that
+    much smaller."""
     cfg = moe.config(T, d, E, k, f, dtype, scale_inputs=scale)
     L = moe.moe_workspace_layout(cfg)
     es = 2 if dtype == "bf16" else 4

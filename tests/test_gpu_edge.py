@@ -26,11 +26,14 @@ def test_one_expert(moe, oracle, dtype):
     check_layer(moe, oracle, w, device="cpu")
 
 
+@pytest.mark.parametrize("scale", [False, True])
 @pytest.mark.parametrize("renorm", [False, True])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_k_equals_E(moe, oracle, dtype, renorm):
-    """k = E: the path with nothing to permute (the experts read x itself)."""
-    w = synth.Workload("dense", 200, 96, 4, 4, 136, dtype, 22, renorm=renorm)
+def test_k_equals_E(moe, oracle, dtype, renorm, scale):
+    """k = E: the path with nothing to permute (the experts read x itself);
+    with the weights on the inputs, bf16 scales each row's products in the
+    first GEMM and fp32 copies scaled rows."""
+    w = synth.Workload("dense", 200, 96, 4, 4, 136, dtype, 22, renorm=renorm, scale_inputs=scale)
     check_layer(moe, oracle, w, device="cpu")
 
 

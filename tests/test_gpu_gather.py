@@ -109,3 +109,27 @@ def test_gathered_rows_against_oracle(moe, oracle, name):
     _, T, d, E, k, f, dead, rare = next(c for c in CASES if c[0] == name)
     w = synth.Workload("gather_" + name, T, d, E, k, f, "bf16", 700 + T)
     check_layer(moe, oracle, w, device="cpu", bias=_bias(E, w.seed, dead, rare))
+
+
+SCALED = [  # name, T, d, E, k, f: weights on the inputs, no permuted copy of x
+    ("gathered_pairs", 2048, 256, 8, 2, 512),     # rows gathered, CTA pairs
+    ("gathered_hybrid", 1024, 512, 16, 2, 384),   # rows gathered, pairs and single CTAs
+    ("dense_pairs", 1024, 256, 8, 8, 256),        # k = E: x itself, 1024 rows per expert
+    ("dense_singles", 40, 192, 4, 4, 320),        # k = E, 40 rows per expert
+]
+
+
+@pytest.mark.parametrize("name,T,d,E,k,f", SCALED, ids=[c[0] for c in SCALED])
+def test_weights_on_inputs_scaled_in_first_gemm(moe, oracle, name, T, d, E, k, f):
+    """Weights on the inputs (the experts receive tokens already scaled by the
+    router score; Transformers docs "Expert parallelism", introduction, the
+    Llama 4 note) where moe_forward forms no permuted copy of x: the dispatch
+    records each row's weight and the first grouped GEMM multiplies the row's
+    gate and up accumulators by it before the SwiGLU, since (w x) W = w (x W)
+    (the oracle forms (w x) W in fp64).  Checked against the oracle; the
+    layout shows no x_perm region."""
+    w = synth.Workload("scaled_" + name, T, d, E, k, f, "bf16", 500 + T + d, renorm=False,
+                       scale_inputs=True)
+    cfg = moe.config(T, d, E, k, f, "bf16", False, scale_inputs=True)
+    assert moe.moe_workspace_layout(cfg).x_perm == moe.MOE_WS_ABSENT
+    check_layer(moe, oracle, w, device="cpu")

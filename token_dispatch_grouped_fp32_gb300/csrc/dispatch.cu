@@ -243,9 +243,12 @@ place_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist,
 
 // Launch 2 when no row moves (x_perm == nullptr: the experts gather the rows
 // themselves): a thread per pair, the same row lookup as place_rows_kernel.
+// With row_scale, also row_scale[row] = w[q] (the weight the experts apply
+// to the row's products).
 __global__ void __launch_bounds__(kThreads)
 place_index_kernel(const int32_t *__restrict__ hist, int64_t P, int k, int chunk, int NB,
-                   int32_t *__restrict__ pos, int32_t *__restrict__ src_token) {
+                   int32_t *__restrict__ pos, int32_t *__restrict__ src_token,
+                   const float *__restrict__ w, float *__restrict__ row_scale) {
     pdl_entry();
     const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     if (q >= P) return;
@@ -254,6 +257,7 @@ place_index_kernel(const int32_t *__restrict__ hist, int64_t P, int k, int chunk
     const int row = hist[(int64_t)(v >> kRankBits) * NB + (int)(q / chunk)] + (v & kRankMask);
     pos[q] = row;
     src_token[row] = (int32_t)(q / k);
+    if (row_scale != nullptr) row_scale[row] = w[q];
 }
 
 // Every token picks every expert (k == E), each once, so expert e's segment
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(kThreads)
 dispatch_all_experts_kernel(const int32_t *__restrict__ idx, int64_t T, int E,
                             int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                             int32_t *__restrict__ pos, int32_t *__restrict__ src_token,
+                            const float *__restrict__ w, float *__restrict__ row_scale,
                             DevStatus ds) {
     pdl_entry();
     const int64_t P = T * E;
@@ -283,6 +288,7 @@ dispatch_all_experts_kernel(const int32_t *__restrict__ idx, int64_t T, int E,
         const int64_t row = (int64_t)e * T + t;
         pos[q] = (int32_t)row;
         src_token[row] = (int32_t)t;
+        if (row_scale != nullptr) row_scale[row] = w[q];
     }
 }
 
@@ -290,11 +296,12 @@ dispatch_all_experts_kernel(const int32_t *__restrict__ idx, int64_t T, int E,
 
 cudaError_t launch_dispatch_all_experts(const Shape &s, const int32_t *idx, int32_t *counts,
                                         int32_t *offsets, int32_t *pos, int32_t *src_token,
-                                        const DevStatus &ds, cudaStream_t st) {
+                                        const DevStatus &ds, cudaStream_t st, const float *w,
+                                        float *row_scale) {
     const int64_t P = s.P();
     const unsigned blocks = (unsigned)std::min<int64_t>((P + kThreads - 1) / kThreads, 4096);
     launch_pdl(dispatch_all_experts_kernel, dim3(blocks), dim3(kThreads), 0, st, idx, s.T, s.E,
-               counts, offsets, pos, src_token, ds);
+               counts, offsets, pos, src_token, w, row_scale, ds);
     return cudaGetLastError();
 }
 
@@ -331,7 +338,7 @@ unsigned *dispatch_ticket(const Shape &s, int32_t *scratch) {
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
-                            const float *scale, bool ticket_zeroed) {
+                            const float *scale, bool ticket_zeroed, float *row_scale) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -358,7 +365,7 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
     if (x_perm == nullptr) {  // pos and src_token only (moe_forward's gathered-row path)
         launch_pdl(place_index_kernel, dim3((unsigned)((P + kThreads - 1) / kThreads)),
                    dim3(kThreads), 0, st, static_cast<const int32_t *>(hist), P, s.k, g.chunk,
-                   g.blocks, pos, src_token);
+                   g.blocks, pos, src_token, scale, scale != nullptr ? row_scale : nullptr);
         return cudaGetLastError();
     }
     const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);

@@ -156,6 +156,10 @@ struct Params {
     int gather;
     const __nv_bfloat16 *gx;
     const int32_t *src_token;
+    // G1 only, or nullptr: row r's gate and up accumulators are multiplied
+    // by row_scale[r] before the SwiGLU (the routing weight acting on the
+    // expert's input row: (w x) W = w (x W))
+    const float *row_scale;
     DevStatus ds;
 };
 
@@ -503,6 +507,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
             const uint32_t t_row = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
             const bool row_ok = r_in_tile < ti.rows;
             __nv_bfloat16 *orow = out + (int64_t)(ti.row0 + r_in_tile) * n_out;
+            const bool scale_rows = sw && p.row_scale != nullptr;  // uniform over the launch
+            const float sc = scale_rows && row_ok ? __ldcg(p.row_scale + ti.row0 + r_in_tile) : 1.f;
             if (transpose) {
                 // rows of this warp: ti.row0 + rank*BM + quarter*32 + (0..31)
                 const int wrow0 = (int)rank * BM + quarter * 32;
@@ -524,6 +530,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                             for (int i = 0; i < 16; ++i) {
                                 float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
                                 float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                                if (scale_rows) {
+                                    g0 *= sc;
+                                    g1 *= sc;
+                                    u0 *= sc;
+                                    u1 *= sc;
+                                }
                                 __nv_bfloat162 b2 = __floats2bfloat162_rn(__fdividef(g0, 1.f + __expf(-g0)) * u0,
                                                                           __fdividef(g1, 1.f + __expf(-g1)) * u1);
                                 packed[16 * half + i] = *reinterpret_cast<uint32_t *>(&b2);
@@ -558,6 +570,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     for (int i = 0; i < 16; ++i) {
                         float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
                         float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+                        if (scale_rows) {
+                            g0 *= sc;
+                            g1 *= sc;
+                            u0 *= sc;
+                            u1 *= sc;
+                        }
                         float h0 = __fdividef(g0, 1.f + __expf(-g0)) * u0;
                         float h1 = __fdividef(g1, 1.f + __expf(-g1)) * u1;
                         __nv_bfloat162 b2 = __floats2bfloat162_rn(h0, h1);
@@ -788,7 +806,10 @@ cudaError_t launch_product(const Shape &s, int units, const CUtensorMap &mx,
     p.experts = experts;
     if (phase == 1) p.g2.n_tiles = 0;
     else p.g1.n_tiles = 0;
-    if (phase == 2) p.gather = 0;  // G2's A (h_perm) is read by TMA
+    if (phase == 2) {
+        p.gather = 0;  // G2's A (h_perm) is read by TMA
+        p.row_scale = nullptr;
+    }
     const int64_t n_tiles = phase == 1 ? both.g1.n_tiles : both.g2.n_tiles;
     const unsigned grid = CTAS * (unsigned)std::min<int64_t>(units, row_tiles_max * n_tiles);
     return launch<CTAS>(grid, mx, mwgu, mh, mwd, p, st);
@@ -832,7 +853,7 @@ bool grouped_swiglu_tc_gather_pays(const Shape &s) {
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
                                      const DevStatus &ds, cudaStream_t st, bool a_local,
-                                     const int32_t *src_token) {
+                                     const int32_t *src_token, const float *row_scale) {
     using namespace tc;
     static DeviceInfo info[64];
     int dev = 0;
@@ -905,6 +926,7 @@ cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const i
     p.gather = gather ? 1 : 0;
     p.gx = static_cast<const __nv_bfloat16 *>(x_perm);
     p.src_token = src_token;
+    p.row_scale = row_scale;
     p.ds = ds;
     // G1 launches, then G2 launches (G2 reads h_perm; stream order)
     const TileMode mode = tile_mode(s);

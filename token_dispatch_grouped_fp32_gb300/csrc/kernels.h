@@ -53,7 +53,7 @@ cudaError_t launch_router_logits_tc(const Shape &s, const void *x, const float *
 
 // Dispatch: chunking of the P pairs over the rank kernel's blocks.
 struct DispatchGrid {
-    int chunk;  // pairs per block (multiple of 256)
+    int chunk;  // pairs per block (a multiple of 256)
     int blocks;  // number of blocks (>= 1 when P > 0)
 };
 DispatchGrid dispatch_grid(int64_t P, int E);
@@ -62,13 +62,15 @@ size_t dispatch_scratch_bytes(const Shape &s);  // count matrix [E][chunks] + ti
 // dispatch's first launch starts; the dispatch leaves it 0).
 unsigned *dispatch_ticket(const Shape &s, int32_t *hist);
 // x_perm == nullptr: counts, offsets, pos and src_token only (no row gather).
-// scale != nullptr: each gathered row is multiplied by its pair's weight.
+// scale != nullptr: each gathered row is multiplied by its pair's weight;
+// without x_perm, row_scale[row] = scale[pair] instead (if row_scale).
 // ticket_zeroed: an earlier kernel in the stream already cleared the ticket;
 // otherwise it is cleared here with a 4-byte cudaMemsetAsync.
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
-                            const float *scale = nullptr, bool ticket_zeroed = false);
+                            const float *scale = nullptr, bool ticket_zeroed = false,
+                            float *row_scale = nullptr);
 
 // Grouped SwiGLU experts.  bf16: tcgen05 tensor-core path; fp32: SIMT path.
 // Kernel launches of one launch_grouped_swiglu_tc call (2, or 4 when the
@@ -82,10 +84,14 @@ bool grouped_swiglu_tc_gather_pays(const Shape &s);
 // reads row r - offsets[e] (every expert receives every token, in order).
 // src_token (not null): x_perm is the T token rows x, and G1 gathers row r
 // of the segments from row src_token[r] (d a multiple of 64, no a_local).
+// row_scale (not null): G1 multiplies row r's gate and up accumulators by
+// row_scale[r] (the routing weight on the expert's input, applied after the
+// product instead of to the rows).
 cudaError_t launch_grouped_swiglu_tc(const Shape &s, const void *x_perm, const int32_t *offsets,
                                      const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
                                      const DevStatus &ds, cudaStream_t st, bool a_local = false,
-                                     const int32_t *src_token = nullptr);
+                                     const int32_t *src_token = nullptr,
+                                     const float *row_scale = nullptr);
 cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const int32_t *offsets,
                                       const float *Wgu, const float *Wd, float *h_perm,
                                       float *y_perm, cudaStream_t st, bool a_local = false);
@@ -93,9 +99,11 @@ cudaError_t launch_grouped_swiglu_f32(const Shape &s, const float *x_perm, const
 // Dispatch when every token picks every expert (k == E): counts[e] = T,
 // offsets[e] = e*T, pos[t*E+j] = idx[t][j]*T + t, src_token[e*T + t] = t.
 // No rows are copied (the experts read x with a_local).  One launch.
+// w, row_scale (both or neither): row_scale[idx[t][j]*T + t] = w[t][j].
 cudaError_t launch_dispatch_all_experts(const Shape &s, const int32_t *idx, int32_t *counts,
                                         int32_t *offsets, int32_t *pos, int32_t *src_token,
-                                        const DevStatus &ds, cudaStream_t st);
+                                        const DevStatus &ds, cudaStream_t st,
+                                        const float *w = nullptr, float *row_scale = nullptr);
 
 // Weighted combine of the expert rows back into token order (w == nullptr:
 // unweighted sum).

@@ -171,17 +171,25 @@ moe_status_t from_cuda(cudaError_t e, const char *what) {
     return MOE_ERR_CUDA;
 }
 
-// k == E with the weights on the outputs: every expert receives every token
-// unscaled, so moe_forward skips the permutation of x (see
-// launch_dispatch_all_experts) and the experts read x directly.
-bool all_experts_path(const Shape &s) { return s.k == s.E && !s.scale_inputs; }
+// k == E: every expert receives every token, so moe_forward skips the
+// permutation of x (see launch_dispatch_all_experts) and the experts read x
+// directly.  With the weights on the inputs this needs the first GEMM to
+// apply them (bf16: rows_scaled_in_gemm); the fp32 path copies scaled rows.
+bool all_experts_path(const Shape &s) { return s.k == s.E && (!s.scale_inputs || s.bf16); }
 
-// bf16 with the weights on the outputs, where the grouped GEMM's row gather
-// pays (grouped_swiglu_tc_gather_pays): the dispatch only ranks and places
-// the pairs, and the first expert GEMM gathers its rows from x through
+// bf16 where the grouped GEMM's row gather pays
+// (grouped_swiglu_tc_gather_pays): the dispatch only ranks and places the
+// pairs, and the first expert GEMM gathers its rows from x through
 // src_token.
 bool gather_path(const Shape &s) {
-    return s.bf16 && !s.scale_inputs && !all_experts_path(s) && grouped_swiglu_tc_gather_pays(s);
+    return s.bf16 && !all_experts_path(s) && grouped_swiglu_tc_gather_pays(s);
+}
+
+// Weights on the inputs with no permuted copy of x (the two paths above):
+// the dispatch records each row's weight (row_scale) and the first GEMM
+// multiplies the row's gate and up accumulators by it, (w x) W = w (x W).
+bool rows_scaled_in_gemm(const Shape &s) {
+    return s.bf16 && s.scale_inputs && (all_experts_path(s) || gather_path(s));
 }
 
 // moe_forward writes and reads x_perm unless its experts read x itself.
@@ -189,7 +197,8 @@ bool forward_uses_x_perm(const Shape &s) { return !all_experts_path(s) && !gathe
 
 // ----- workspace layout of moe_forward (256-byte aligned sub-buffers) -----
 struct WsLayout {
-    size_t logits, idx, w, counts, offsets, pos, src, hist, route, x_perm, h_perm, y_perm, total;
+    size_t logits, idx, w, counts, offsets, pos, src, hist, route, row_scale, x_perm, h_perm,
+        y_perm, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -207,6 +216,8 @@ WsLayout ws_layout(const Shape &s) {
     L.src = o;    o = up256(o + 4 * P);
     L.hist = o;   o = up256(o + dispatch_scratch_bytes(s));
     L.route = o;  o = up256(o + router_tc_scratch_bytes(s));
+    L.row_scale = o;
+    if (rows_scaled_in_gemm(s)) o = up256(o + 4 * P);
     if (forward_uses_x_perm(s)) {
         L.x_perm = o;
         o = up256(o + es * P * s.d);
@@ -252,14 +263,15 @@ moe_status_t run_route(const Shape &s, const void *x, const float *Wr, const flo
 
 // a_local: x_perm is x itself, every segment the T tokens in order (k == E).
 // src_token (bf16 only): x_perm is x itself and G1 gathers its rows.
+// row_scale (bf16 only): G1 scales row r's products by row_scale[r].
 moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offsets,
                          const void *Wgu, const void *Wd, void *h_perm, void *y_perm,
                          const DevStatus &ds, cudaStream_t st, bool a_local = false,
-                         const int32_t *src_token = nullptr) {
+                         const int32_t *src_token = nullptr, const float *row_scale = nullptr) {
     cudaError_t e;
     if (s.bf16)
         e = launch_grouped_swiglu_tc(s, x_perm, offsets, Wgu, Wd, h_perm, y_perm, ds, st, a_local,
-                                     src_token);
+                                     src_token, row_scale);
     else
         e = launch_grouped_swiglu_f32(s, static_cast<const float *>(x_perm), offsets,
                                       static_cast<const float *>(Wgu),
@@ -487,21 +499,24 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
     int32_t *hist = at<int32_t>(ws, L.hist);
     const bool all_experts = all_experts_path(s);
     const bool gather = gather_path(s);
+    float *row_scale = rows_scaled_in_gemm(s) ? at<float>(ws, L.row_scale) : nullptr;
     // the route's last launch clears the dispatch's ticket counter
     if ((st = run_route(s, x, Wr, logit_bias, logits, idx, w, at<uint8_t>(ws, L.route), ds, cs,
                         all_experts ? nullptr : dispatch_ticket(s, hist))) != MOE_OK)
         return st;
     if (all_experts)
-        st = from_cuda(launch_dispatch_all_experts(s, idx, counts, offsets, pos, src, ds, cs),
+        st = from_cuda(launch_dispatch_all_experts(s, idx, counts, offsets, pos, src, ds, cs,
+                                                   row_scale ? w : nullptr, row_scale),
                        "dispatch launch");
     else
         st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src,
                                        gather ? nullptr : x_perm, hist, ds, cs,
-                                       s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true),
+                                       s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true,
+                                       row_scale),
                        "dispatch launch");
     if (st != MOE_OK) return st;
     if ((st = run_experts(s, all_experts || gather ? x : x_perm, offsets, W_gate_up, W_down, h_perm,
-                          y_perm, ds, cs, all_experts, gather ? src : nullptr)) != MOE_OK)
+                          y_perm, ds, cs, all_experts, gather ? src : nullptr, row_scale)) != MOE_OK)
         return st;
     return from_cuda(launch_combine(s, y_perm, pos, s.scale_inputs ? nullptr : w, out, cs),
                      "combine launch");
