@@ -46,6 +46,10 @@ CASES = [  # name, T, d, E, k, f, dead expert, rare expert and its logit offset
     ("hybrid", 1024, 512, 16, 2, 384, 7, None),     # 128 rows per expert on average
     ("singles", 64, 192, 32, 4, 256, None, None),   # 8 rows per expert on average
     ("pairs_k8", 4096, 128, 64, 8, 2048, 0, None),  # f at the gather's limit
+    ("one_k_step", 1536, 64, 4, 2, 192, None, None),  # d = 64: one K step per tile
+    ("two_experts", 1400, 128, 2, 1, 256, None, None),  # E = 2, k = 1: pairs, two segments
+    ("one_token", 1, 256, 16, 4, 512, None, None),    # T = 1: four rows, one per expert
+    ("many_experts", 2048, 128, 1024, 2, 64, None, None),  # E = 1024, about 4 rows each
 ]
 
 
