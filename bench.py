@@ -415,6 +415,9 @@ def measure_workload(moe, w, args, dev, rank, world, flush, with_e2e):
         "combine": {"ms": kms["combine"], "GB/s": comb_bytes / kms["combine"] / 1e6,
                     "frac_hbm": comb_bytes / kms["combine"] / 1e6 / hbm},
         "sum_ms": sum(kms.values()), "same_output_as_moe_forward": same_as_fused,
+        "breakdown": "the component entry points (route, dispatch with its row copy, grouped "
+                     "GEMMs, combine), timed one by one",
+        "forward_path": forward_path(moe, cfg, w),
     }
     roofline = {"bound": "tensor", "achieved": gemm_tflops, "peak": peak,
                 "unit": "TFLOP/s", "frac": gemm_tflops / peak,
@@ -502,6 +505,7 @@ def workload_summary(r):
             "dispatch": {"ms": k["dispatch"]["ms"], "frac_hbm": k["dispatch"]["frac_hbm"]},
             "combine": {"ms": k["combine"]["ms"], "frac_hbm": k["combine"]["frac_hbm"]},
             "same_output_as_moe_forward": k["same_output_as_moe_forward"],
+            "forward_path": k["forward_path"],
             "gpu_launches_per_step": r["launches_per_step"], "clocks": r["clocks"]}
 
 
@@ -565,6 +569,23 @@ def run_ours(args, w):
     if world > 1 and dist.is_initialized():
         dist.destroy_process_group()
     return line
+
+
+def forward_path(moe, cfg, w):
+    """How moe_forward moves the rows for this config, from the library's own
+    workspace layout (an absent x_perm region: no permuted copy of x)."""
+    copied = moe.moe_workspace_layout(cfg).x_perm != moe.MOE_WS_ABSENT
+    if copied:
+        return ("rows copied into x_perm" +
+                (", scaled by their weights" if w.scale_inputs else "") +
+                "; the same arithmetic as the component entry points")
+    how = ("every expert reads x itself (k = E)" if w.k == w.E
+           else "the first grouped GEMM gathers its rows from x through src_token")
+    if w.scale_inputs:
+        return how + "; the weights scale each row's gate and up products in fp32 inside the " \
+                     "first grouped GEMM (the component path rounds w*x to bf16 first, so the " \
+                     "outputs differ within the rounding)"
+    return how + "; bit-identical to the component entry points"
 
 
 def recorded_traffic(w):

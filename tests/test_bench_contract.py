@@ -66,3 +66,23 @@ def test_layer_roofline_is_the_slower_bound():
     nbytes = 111 * 3 * 2880 * 2880 * 2 + 2 * 64 * 2880 * 2 + 4 * 128 * 2880
     assert r["bytes"] == nbytes and r["bound"] == "hbm"
     assert abs(r["frac"] - nbytes / 6777e9 / 0.85e-3) < 1e-12
+
+
+def test_forward_path_follows_the_workspace_layout():
+    """The bench's description of how moe_forward moves the rows comes from
+    the library's layout query (no x_perm region: no permuted copy)."""
+    import bench
+    from token_dispatch_grouped_fp32_gb300 import moe, synth
+
+    def path(name, **kw):
+        w = synth.WORKLOADS[name].with_(**kw)
+        cfg = moe.config(w.T, w.d, w.E, w.k, w.f, w.dtype, w.renorm, scale_inputs=w.scale_inputs)
+        return bench.forward_path(moe, cfg, w)
+
+    assert path("mixtral").startswith("rows copied into x_perm")
+    assert "scaled by their weights" in path("mixtral", scale_inputs=True)
+    assert path("qwen3_zipf").startswith("the first grouped GEMM gathers")
+    assert "bit-identical" in path("deepseek")
+    assert "inside the first grouped GEMM" in path("qwen3_zipf", scale_inputs=True)
+    assert path("mixtral_dense").startswith("every expert reads x itself")
+    assert path("tiny_fp32").startswith("rows copied")  # fp32: no gather
