@@ -259,7 +259,10 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int *s_off, cons
 }
 
 // tmX / tmWgu: A and B of G1; tmH / tmWd: A and B of G2.
-template <int CTAS, bool GATHER>
+// SCALE: G1 multiplies each row's gate and up accumulators by
+// Params::row_scale (a separate instantiation, so launches without row
+// scales run the epilogue without the extra branch).
+template <int CTAS, bool GATHER, bool SCALE>
 __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmWgu,
@@ -507,8 +510,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
             const uint32_t t_row = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quarter * 32) << 16);
             const bool row_ok = r_in_tile < ti.rows;
             __nv_bfloat16 *orow = out + (int64_t)(ti.row0 + r_in_tile) * n_out;
-            const bool scale_rows = sw && p.row_scale != nullptr;  // uniform over the launch
-            const float sc = scale_rows && row_ok ? __ldcg(p.row_scale + ti.row0 + r_in_tile) : 1.f;
+            float sc = 1.f;  // the row's weight (SCALE launches hold G1 tiles only)
+            if constexpr (SCALE)
+                if (row_ok) sc = __ldcg(p.row_scale + ti.row0 + r_in_tile);
             if (transpose) {
                 // rows of this warp: ti.row0 + rank*BM + quarter*32 + (0..31)
                 const int wrow0 = (int)rank * BM + quarter * 32;
@@ -530,7 +534,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                             for (int i = 0; i < 16; ++i) {
                                 float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
                                 float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-                                if (scale_rows) {
+                                if constexpr (SCALE) {
                                     g0 *= sc;
                                     g1 *= sc;
                                     u0 *= sc;
@@ -570,7 +574,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX,
                     for (int i = 0; i < 16; ++i) {
                         float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
                         float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-                        if (scale_rows) {
+                        if constexpr (SCALE) {
                             g0 *= sc;
                             g1 *= sc;
                             u0 *= sc;
@@ -740,39 +744,54 @@ cudaLaunchConfig_t launch_config(unsigned grid, cudaStream_t st, cudaLaunchAttri
     return cfg;
 }
 
+template <int CTAS, bool GATHER, bool SCALE>
+cudaError_t launch_variant(unsigned grid, const CUtensorMap &mx, const CUtensorMap &mwgu,
+                           const CUtensorMap &mh, const CUtensorMap &mwd, const Params &p,
+                           cudaStream_t st) {
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg =
+        launch_config<CTAS>(grid, st, attr, GATHER ? NUM_THREADS_GATHER : NUM_THREADS);
+    return cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS, GATHER, SCALE>, mx, mwgu, mh, mwd,
+                              p);
+}
+
 template <int CTAS>
 cudaError_t launch(unsigned grid, const CUtensorMap &mx, const CUtensorMap &mwgu,
                    const CUtensorMap &mh, const CUtensorMap &mwd, const Params &p,
                    cudaStream_t st) {
-    cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        launch_config<CTAS>(grid, st, attr, p.gather ? NUM_THREADS_GATHER : NUM_THREADS);
-    return p.gather ? cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS, true>, mx, mwgu, mh, mwd, p)
-                    : cudaLaunchKernelEx(&cfg, grouped_gemm_tc_kernel<CTAS, false>, mx, mwgu, mh, mwd, p);
+    const bool scale = p.row_scale != nullptr;
+    if (p.gather)
+        return scale ? launch_variant<CTAS, true, true>(grid, mx, mwgu, mh, mwd, p, st)
+                     : launch_variant<CTAS, true, false>(grid, mx, mwgu, mh, mwd, p, st);
+    return scale ? launch_variant<CTAS, false, true>(grid, mx, mwgu, mh, mwd, p, st)
+                 : launch_variant<CTAS, false, false>(grid, mx, mwgu, mh, mwd, p, st);
 }
 
-// Both instantiations fit one CTA per SM (shared memory); the resident
-// count is the smaller of the two.
-template <int CTAS> cudaError_t prepare(int *resident_units) {
-    cudaError_t err;
-    if ((err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS, false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<CTAS>::SMEM_BYTES)) != cudaSuccess ||
-        (err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS, true>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Cfg<CTAS>::SMEM_BYTES)) != cudaSuccess)
-        return err;
+// Shared-memory opt-in and the clusters (or CTAs) resident at once for one
+// instantiation; every instantiation fits one CTA per SM.
+template <int CTAS, bool GATHER, bool SCALE> cudaError_t prepare_variant(int *resident_units) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_tc_kernel<CTAS, GATHER, SCALE>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Cfg<CTAS>::SMEM_BYTES);
+    if (err != cudaSuccess) return err;
     cudaLaunchAttribute attr[2];
-    int a = 0, b = 0;
-    cudaLaunchConfig_t cfg = launch_config<CTAS>(CTAS, nullptr, attr, NUM_THREADS);
-    if ((err = cudaOccupancyMaxActiveClusters(&a, grouped_gemm_tc_kernel<CTAS, false>, &cfg)) !=
-        cudaSuccess)
+    cudaLaunchConfig_t cfg =
+        launch_config<CTAS>(CTAS, nullptr, attr, GATHER ? NUM_THREADS_GATHER : NUM_THREADS);
+    return cudaOccupancyMaxActiveClusters(resident_units,
+                                          grouped_gemm_tc_kernel<CTAS, GATHER, SCALE>, &cfg);
+}
+
+// The resident count used for the grid is the smallest over the
+// instantiations.
+template <int CTAS> cudaError_t prepare(int *resident_units) {
+    int n[4] = {0, 0, 0, 0};
+    cudaError_t err;
+    if ((err = prepare_variant<CTAS, false, false>(&n[0])) != cudaSuccess ||
+        (err = prepare_variant<CTAS, false, true>(&n[1])) != cudaSuccess ||
+        (err = prepare_variant<CTAS, true, false>(&n[2])) != cudaSuccess ||
+        (err = prepare_variant<CTAS, true, true>(&n[3])) != cudaSuccess)
         return err;
-    cfg = launch_config<CTAS>(CTAS, nullptr, attr, NUM_THREADS_GATHER);
-    if ((err = cudaOccupancyMaxActiveClusters(&b, grouped_gemm_tc_kernel<CTAS, true>, &cfg)) !=
-        cudaSuccess)
-        return err;
-    *resident_units = std::min(a, b);
+    *resident_units = std::min(std::min(n[0], n[1]), std::min(n[2], n[3]));
     return cudaSuccess;
 }
 
