@@ -283,7 +283,7 @@ moe_status_t moe_combine(const moe_config_t *cfg, const void *y_perm,
  * the dispatch only writes counts, offsets, pos and src_token, and the first
  * grouped GEMM reads the rows of x itself instead of x_perm (for fp32 with
  * the weights on the inputs, the scaled rows are copied instead).
- * Otherwise, for bf16 activations with d a multiple of 64 and f <= 2048, the
+ * Otherwise, for bf16 activations with d a multiple of 64 and f <= 3072, the
  * permuted copy of x is not formed either: the dispatch writes counts,
  * offsets, pos and src_token, and the first grouped GEMM gathers row r of
  * the segments from x[src_token[r]] itself (measured faster there than

@@ -195,6 +195,8 @@ def test_wait_limit_has_a_floor_outside_the_test_hook(moe):
 @pytest.mark.parametrize("T,d,E,k,f,dtype,scale,x_perm", [
     (4096, 4096, 8, 2, 14336, "bf16", False, True),   # f > 2048: the permuted copy
     (8192, 7168, 256, 8, 2048, "bf16", False, False),  # gathered rows
+    (8192, 2880, 128, 4, 2880, "bf16", False, False),  # gathered rows, f at 2880
+    (8192, 2880, 128, 4, 3136, "bf16", False, True),   # f above the gather's limit: copied
     (8192, 7168, 256, 8, 2048, "bf16", True, False),   # weights on the inputs: still gathered
     (4096, 4096, 8, 2, 14336, "bf16", True, True),     # weights on the inputs, f > 2048: scaled copy
     (8192, 7200, 256, 8, 2048, "bf16", False, True),   # d not a multiple of 64
@@ -207,7 +209,7 @@ def test_workspace_layout(moe, T, d, E, k, f, dtype, scale, x_perm):
     aligned, in order, large enough for their arrays, and inside the total;
     x_perm is absent exactly where moe_forward forms no permuted copy of x
     (k == E, except fp32 with the weights on the inputs; or the gathered-row
-    path: bf16, d a multiple of 64, f <= 2048), and the total is then that
+    path: bf16, d a multiple of 64, f <= 3072), and the total is then that
     much smaller."""
     cfg = moe.config(T, d, E, k, f, dtype, scale_inputs=scale)
     L = moe.moe_workspace_layout(cfg)

@@ -83,6 +83,7 @@ def test_forward_path_follows_the_workspace_layout():
     assert "scaled by their weights" in path("mixtral", scale_inputs=True)
     assert path("qwen3_zipf").startswith("the first grouped GEMM gathers")
     assert "bit-identical" in path("deepseek")
+    assert path("gptoss_prefill").startswith("the first grouped GEMM gathers")
     assert "inside the first grouped GEMM" in path("qwen3_zipf", scale_inputs=True)
     assert path("mixtral_dense").startswith("every expert reads x itself")
     assert path("tiny_fp32").startswith("rows copied")  # fp32: no gather

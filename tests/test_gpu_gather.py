@@ -1,7 +1,7 @@
 """The gathered-row path of moe_forward against the copying path.
 
 For bf16 activations with the weights on the outputs, d a multiple of 64 and
-f <= 2048, moe_forward forms no permuted copy of x: the dispatch writes only
+f <= 3072, moe_forward forms no permuted copy of x: the dispatch writes only
 counts, offsets, pos and src_token, and the first grouped GEMM's extra warps
 copy each A row of a stage from x[src_token[row]] into the swizzled shared
 memory layout the tensor memory access (TMA) unit would have written

@@ -860,11 +860,12 @@ bool grouped_swiglu_tc_gathers(const Shape &s) { return s.d % tc::BK == 0; }
 // Gathering G1's rows saves the permuted copy of x (written once, read once)
 // and costs the gather kernel's throughput (its extra warps hold the block's
 // registers to 168 a thread, and its copies share the SM's intake with the
-// weight tiles).  The saving per FLOP falls as 1/f; measured against the
-// copying path, the layer ran 3-6 % faster at f = 768 (Qwen3-30B-A3B
-// shape), 1.4 % at f = 2048 (DeepSeek-V3 shape), no faster at f = 2880
-// (gpt-oss) and 3 % slower at f = 14336 (Mixtral shape).
-constexpr int kGatherMaxF = 2048;
+// weight tiles).  The saving per FLOP falls as 1/f.  Measured against the
+// copying path: the Qwen3-30B-A3B shape (f = 768) 3-7 % faster, the
+// DeepSeek-V3 shape (f = 2048) 1.4-2.7 %, gpt-oss (f = 2880) 0.9 % in short
+// runs at full clock and 0.1-0.4 % slower under the power cap, the Mixtral
+// shape (f = 14336) 1.3-4 % slower.
+constexpr int kGatherMaxF = 3072;
 bool grouped_swiglu_tc_gather_pays(const Shape &s) {
     return grouped_swiglu_tc_gathers(s) && s.f <= kGatherMaxF;
 }
