@@ -115,8 +115,13 @@ def test_deterministic(moe):
     assert torch.equal(a, b)
 
 
-def test_cuda_graph_capture(moe):
-    layer, x = _layer(moe, "gptoss_prefill", 1000)
+@pytest.mark.parametrize("name,T", [("gptoss_prefill", 1000),  # rows gathered in G1
+                                    ("mixtral", 512),           # rows copied into x_perm
+                                    ("mixtral_dense", 128)])    # k = E: x itself
+def test_cuda_graph_capture(moe, name, T):
+    """moe_forward needs no host synchronisation, so a captured graph replays
+    it with the same result, on each of the ways it moves the rows."""
+    layer, x = _layer(moe, name, T)
     ref = layer(x).clone()
     out = torch.empty_like(x)
     s = torch.cuda.Stream()
