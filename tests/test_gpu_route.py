@@ -33,6 +33,12 @@ ROUTE_CASES = [
     (200, 3, 3, None),
     (50, 64, 6, "all_equal"),
     (8192, 256, 8, None),
+    # T >= 1024 with E <= 256 takes the sorted-heads selection: ties there too
+    (2048, 128, 8, "coarse"),
+    (1024, 256, 8, "coarse"),
+    (1536, 48, 5, "coarse"),
+    (1500, 64, 6, "all_equal"),
+    (1024, 200, 7, None),
 ]
 
 
@@ -170,3 +176,36 @@ def test_route_tensor_core_shapes(moe, oracle, T, d, E, k):
     ref_idx, ref_w = oracle.topk(logits.cpu().numpy(), k, True)
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
     assert np.abs(wt.cpu().numpy().astype(np.float64) - ref_w).max() <= weight_tolerance(E)
+
+
+@pytest.mark.parametrize("T", [37, 1100])  # the plain selection; the sorted-heads one
+@pytest.mark.parametrize("E,k", [(8, 6), (64, 24), (128, 32), (256, 32)])
+def test_route_special_values_match_oracle(moe, oracle, T, E, k):
+    """Signed zeros tie (the lower id wins), -inf ranks below every finite
+    value and a NaN below everything, a later NaN losing to an earlier one.
+    About half of each row's k picks are finite, so the selection reaches
+    into the -inf and (on half the rows) the NaN entries.  Indices bit for
+    bit against the oracle on the same buffer; weights too on the rows
+    without a NaN and with a finite logit."""
+    g = np.random.default_rng(4000 + T + E)
+    L = np.round(g.standard_normal((T, E)) * 2.0) / 2.0  # many exact ties
+    L[g.random((T, E)) < 0.15] = 0.0
+    L[g.random((T, E)) < 0.15] = -0.0
+    special = g.random((T, E)) < 1.0 - k / (2.0 * E)
+    nan_rows = g.random(T) < 0.5
+    as_nan = special & nan_rows[:, None] & (g.random((T, E)) < 0.85)
+    L[special] = -np.inf
+    L[as_nan] = np.nan
+    L = L.astype(np.float32)
+    cfg = moe.config(T, 8, E, k, 8, "f32", True)
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, k), -7.0, dtype=torch.float32, device="cuda")
+    moe.moe_route_from_logits(cfg, torch.from_numpy(L).cuda(), idx, w)
+    torch.cuda.synchronize()
+    ref_idx, ref_w = oracle.topk(L, k, True)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    # weights are defined where no logit is NaN and some logit is finite
+    clean = ~np.isnan(L).any(axis=1) & np.isfinite(L).any(axis=1)
+    assert clean.any() and (~clean).any()
+    got_w = w.cpu().numpy().astype(np.float64)[clean]
+    assert np.abs(got_w - ref_w[clean]).max() <= weight_tolerance(E)

@@ -332,7 +332,10 @@ cudaError_t launch_logits_t(const Shape &s, const TA *x, const float *Wr, const 
 // warp arg-max under the rank order pick the experts; slot j is written by
 // lane j.  Each round is two warp reductions (redux.sync): the maximum of the
 // values' order-preserving 32-bit images, then the minimum expert id among
-// the still-available values that reach it (the lower id wins ties).
+// the still-available values that reach it (the lower id wins ties).  With
+// SORTED (up to 8 values a lane, E <= 256, and batches large enough that the
+// kernel is bound by instruction issue rather than latency) the lane sorts
+// its values once, so a round looks at each lane's head only.
 // Weights: softmax over all E logits (max-shifted), then optional
 // renormalisation over the chosen k.
 // ---------------------------------------------------------------------------
@@ -353,7 +356,7 @@ __device__ __forceinline__ float rank_value(uint32_t o) {
 // With nparts > 0 the logits are first formed as the sum of nparts partial
 // buffers (stride T*E, added in buffer order) plus bias, and written to
 // `logits`; the selection then uses exactly the written values.
-template <int VPL>
+template <int VPL, bool SORTED>
 __global__ void __launch_bounds__(256)
 topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int nparts,
             const float *__restrict__ bias, int64_t T, int E, int k, int renorm,
@@ -406,6 +409,50 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
     float my_v = 0.f;
     int my_e = 0;
     uint32_t top = 0u;  // the first round's maximum: the largest logit
+    if constexpr (SORTED) {
+        // Each lane first sorts its values (rank image descending, expert id
+        // ascending among equal images), so a round compares the lanes'
+        // heads only, and the lane whose head is chosen shifts its list.
+        // Entries past E rank lowest with the largest id: a valid expert
+        // (a NaN logit included) always wins over them.
+        uint32_t key[VPL], id[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const bool ok = (avail >> i) & 1u;
+            key[i] = ok ? ord[i] : 0u;
+            id[i] = ok ? (uint32_t)(lane + 32 * i) : 0xFFFFFFFFu;
+        }
+#pragma unroll
+        for (int pass = 0; pass < VPL; ++pass) {  // odd-even transposition sort
+#pragma unroll
+            for (int i = pass & 1; i + 1 < VPL; i += 2) {
+                const bool swap = key[i] < key[i + 1] || (key[i] == key[i + 1] && id[i] > id[i + 1]);
+                const uint32_t k0 = key[i], i0 = id[i];
+                key[i] = swap ? key[i + 1] : k0;
+                id[i] = swap ? id[i + 1] : i0;
+                key[i + 1] = swap ? k0 : key[i + 1];
+                id[i + 1] = swap ? i0 : id[i + 1];
+            }
+        }
+        for (int j = 0; j < k; ++j) {
+            const uint32_t omax = __reduce_max_sync(0xffffffffu, key[0]);
+            const uint32_t be = __reduce_min_sync(0xffffffffu, key[0] == omax ? id[0] : 0xFFFFFFFFu);
+            if (id[0] == be) {  // this lane's head was chosen: drop it
+#pragma unroll
+                for (int i = 0; i + 1 < VPL; ++i) {
+                    key[i] = key[i + 1];
+                    id[i] = id[i + 1];
+                }
+                key[VPL - 1] = 0u;
+                id[VPL - 1] = 0xFFFFFFFFu;
+            }
+            if (j == 0) top = omax;
+            if (lane == j) {
+                my_v = rank_value(omax);
+                my_e = (int)be;
+            }
+        }
+    } else
     for (int j = 0; j < k; ++j) {
         // every round has an available value somewhere in the warp (j < k <= E)
         uint32_t lmax = 0u;
@@ -448,13 +495,21 @@ topk_kernel(float *__restrict__ logits, const float *__restrict__ partial, int n
     }
 }
 
+// Sorted heads pay from about this many tokens (measured: T = 4096-16384
+// 1-9 % faster routes; T = 64 1.7 us slower, where the kernel is latency bound).
+constexpr int64_t kTopkSortedMinT = 1024;
+
 template <int VPL>
 cudaError_t launch_topk_v(const Shape &s, float *logits, const float *partial, int nparts,
                           const float *bias, int32_t *idx, float *w, cudaStream_t st,
                           unsigned *zero_word) {
     unsigned blocks = (unsigned)((s.T + 7) / 8);
-    launch_pdl(topk_kernel<VPL>, dim3(blocks), dim3(256), 0, st, logits, partial, nparts, bias, s.T,
-               s.E, s.k, s.renorm ? 1 : 0, idx, w, zero_word);
+    if (VPL <= 8 && s.T >= kTopkSortedMinT)
+        launch_pdl(topk_kernel<VPL, (VPL <= 8)>, dim3(blocks), dim3(256), 0, st, logits, partial,
+                   nparts, bias, s.T, s.E, s.k, s.renorm ? 1 : 0, idx, w, zero_word);
+    else
+        launch_pdl(topk_kernel<VPL, false>, dim3(blocks), dim3(256), 0, st, logits, partial, nparts,
+                   bias, s.T, s.E, s.k, s.renorm ? 1 : 0, idx, w, zero_word);
     return cudaGetLastError();
 }
 
