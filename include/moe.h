@@ -135,8 +135,8 @@ size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
 
 /*
  * Number of kernel launches one moe_forward call makes for `cfg`: the router
- * (1 to 3 launches, by path), the dispatch (2; 1 when k == E without
- * scale_inputs), the two grouped GEMMs (2, or
+ * (1 to 3 launches, by path), the dispatch (2; 1 when k == E, except for
+ * fp32 with scale_inputs), the two grouped GEMMs (2, or
  * 4 when bf16 experts average 64 to 511 rows each and are split between two
  * tile shapes) and the combine (1).  0 when T == 0; -1 for an invalid
  * configuration.  Makes no CUDA call.
