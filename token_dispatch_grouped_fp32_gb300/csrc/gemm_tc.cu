@@ -16,7 +16,13 @@
 // One launch per product when one tile shape serves every expert; two when
 // the experts are split between the shapes (see tile_mode).
 //
-// Tiling.  Two tile shapes share one kernel template (CTAS = 1 or 2).
+// The kernel template is grouped_gemm_tc_kernel<CTAS, GATHER, SCALE>: the
+// tile shape (below), whether G1 gathers its own A rows (GATHER, below), and
+// whether G1 multiplies each row's gate and up accumulators by a per-row
+// weight before the SwiGLU (SCALE: routing weights on the expert inputs,
+// (w x) W = w (x W)).  Each launch runs the instantiation it needs.
+//
+// Tiling.  Two tile shapes share the kernel template (CTAS = 1 or 2).
 //  - CTAS = 2 (a cluster of 2, tcgen05.mma.cta_group::2): the pair owns a
 //    256-row x 256-column tile; each CTA holds its 128 rows of A and half of
 //    the 256 B columns in its own shared memory, and the leader CTA's MMA
@@ -52,7 +58,8 @@
 // proxy fence, then an arrival or, in a pair, a 16-byte async copy into the
 // leader whose bytes complete the stage's full barrier).
 //
-// Roles (192 threads per CTA): one thread of warp 0 issues the TMA loads,
+// Roles (192 threads per CTA; 288 with GATHER, warps 6-8 as above): one
+// thread of warp 0 issues the TMA loads,
 // warp 1 owns the tensor memory and one of its threads issues the MMAs and
 // their commits (in a pair: the leader only, commits multicast to both CTAs,
 // and every load of both CTAs signals the leader's full barrier), warps 2-5
