@@ -280,7 +280,6 @@ moe_status_t run_experts(const Shape &s, const void *x_perm, const int32_t *offs
     return from_cuda(e, "grouped SwiGLU launch");
 }
 
-
 }  // namespace
 }  // namespace moe
 
