@@ -52,6 +52,10 @@ def test_workspace_sizes(moe):
     # P = 8192 pairs in chunks of 256 (the smallest chunk that keeps <= 256 chunks):
     # the [E][chunks] count matrix, then the rank kernel's ticket (16 bytes)
     assert moe.moe_dispatch_workspace_size(cfg) == 4 * 8 * (P // 256) + 16
+    # 40,000 pairs: 128 experts x 157 chunks of 256 would exceed 4096 entries,
+    # so chunks of 2048: a [128][20] count matrix
+    mid = moe.config(5000, 64, 128, 8, 64)
+    assert moe.moe_dispatch_workspace_size(mid) == 4 * 128 * 20 + 16
     big = moe.config(70000, 8, 1024, 8, 8)  # 560,000 pairs: chunks of 2048
     assert moe.moe_dispatch_workspace_size(big) == 4 * 1024 * ((560000 + 2047) // 2048) + 16
     # invalid config -> 0

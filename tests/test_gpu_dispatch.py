@@ -46,7 +46,11 @@ DISPATCH_CASES = [
     # T, E, k, d, dtype, skew
     (1, 8, 2, 64, torch.bfloat16, 0.0),
     (100, 8, 2, 64, torch.bfloat16, 0.0),
-    (3000, 8, 2, 64, torch.float32, 0.0),      # 3 chunks, ragged tail
+    (3000, 8, 2, 64, torch.float32, 0.0),      # 24 chunks, ragged tail
+    (8192, 32, 2, 64, torch.bfloat16, 0.0),    # 64 chunks of 256 (2048 counts)
+    (3, 1024, 8, 16, torch.bfloat16, 0.0),     # a single chunk, E = 1024
+    (1500, 33, 4, 64, torch.bfloat16, 0.0),    # 24 chunks, E not a multiple of 8
+    (8193, 32, 2, 64, torch.bfloat16, 0.0),    # 65 chunks, the last of 2 pairs
     (5000, 128, 8, 32, torch.bfloat16, 0.0),   # 20 chunks
     (2049, 1, 1, 16, torch.bfloat16, 0.0),     # single expert
     (1000, 64, 6, 24, torch.bfloat16, 0.0),
@@ -71,8 +75,9 @@ def test_dispatch_matches_oracle(moe, oracle, T, E, k, d, dtype, skew):
     assert torch.equal(x_perm, x[torch.from_numpy(rs).long()])
 
 
-def test_dispatch_flags_out_of_range_expert(moe, oracle):
-    T, E, k = 50, 8, 2
+@pytest.mark.parametrize("T", [50, 20000])  # one chunk / 157 chunks of 256
+def test_dispatch_flags_out_of_range_expert(moe, oracle, T):
+    E, k = 8, 2
     idx = _routing(oracle, T, E, k, 5)
     idx[7, 1] = E + 3
     x = torch.randn(T, 16).to(torch.bfloat16)

@@ -17,22 +17,29 @@
 // offsets, and resets the ticket for the next call.
 // Launch 2 (place_rows_kernel), one warp per pair: row = first row of the
 // pair's (expert, chunk) + its rank; writes pos, src_token and copies the
-// token's row into x_perm.  Without x_perm (the experts gather the rows),
-// place_index_kernel does the same lookup with a thread per pair.
+// token's row into x_perm.  A standalone dispatch with unscaled rows of at
+// most 16 KB uses place_token_rows_kernel instead, a warp per token, which
+// reads the token's row while launch 1 still runs.  Without x_perm (the
+// experts gather the rows), place_index_kernel does the lookup alone, a
+// thread per pair.
 // Stability: rows of one expert are in ascending pair id, hence ascending
 // token id, and no atomic decides any order.
 #include <algorithm>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kThreads = 256;      // place_rows_kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kRankThreads = 1024;  // rank_kernel
+constexpr int kTokWarps = 4;              // place_token_rows_kernel: tokens per block
+constexpr int kStageRowMax = 16 * 1024;   // its largest row, staged in shared memory
+constexpr int kRankThreads = 1024;  // rank_kernel (256 for chunks of 256 pairs)
 constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kSmallRankThreads = 256;
 // The count matrix is staged in shared memory for the scan when it has at
 // most this many entries (else the scan reads it through L2).
 constexpr int kScanStageMax = 16 * 1024;
@@ -43,24 +50,26 @@ constexpr int kRankBits = 21;
 constexpr int kRankMask = (1 << kRankBits) - 1;
 
 // Exclusive scan, in place, of the expert-major count matrix hist[0 .. E*NB)
-// by one block of kRankThreads: afterwards hist[e*NB + b] is the first row
+// by one block of NT threads: afterwards hist[e*NB + b] is the first row
 // of expert e's pairs in chunk b, counts[e] and offsets[0..E] follow.  The
 // matrix was written by other blocks of the grid, so it is read through L2;
 // `stage` (shared memory for kScanStageMax ints, or nullptr) holds a copy
 // while it is scanned, so the per-thread walks read shared memory.
+template <int NT>
 __device__ void scan_count_matrix(int32_t *__restrict__ hist_g, int E, int NB,
                                   int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                                   int *stage) {
-    __shared__ int warp_tot[kRankWarps];
+    constexpr int NW = NT / 32;
+    __shared__ int warp_tot[NW];
     __shared__ int total_s;
     const int n = E * NB;
     int32_t *hist = hist_g;
     if (stage != nullptr) {
-        for (int i = threadIdx.x; i < n; i += kRankThreads) stage[i] = __ldcg(hist_g + i);
+        for (int i = threadIdx.x; i < n; i += NT) stage[i] = __ldcg(hist_g + i);
         __syncthreads();
         hist = stage;
     }
-    const int seg = (n + kRankThreads - 1) / kRankThreads;
+    const int seg = (n + NT - 1) / NT;
     const int beg = min(n, (int)threadIdx.x * seg);
     const int end = min(n, beg + seg);
     int local = 0;
@@ -75,14 +84,14 @@ __device__ void scan_count_matrix(int32_t *__restrict__ hist_g, int E, int NB,
     if (lane == 31) warp_tot[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-        const int v = warp_tot[lane];  // kRankWarps == 32
+        const int v = lane < NW ? warp_tot[lane] : 0;
         int inc = v;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const int u = __shfl_up_sync(0xffffffffu, inc, off);
             if (lane >= off) inc += u;
         }
-        warp_tot[lane] = inc - v;  // exclusive warp base
+        if (lane < NW) warp_tot[lane] = inc - v;  // exclusive warp base
         if (lane == 31) total_s = inc;
     }
     __syncthreads();
@@ -94,9 +103,9 @@ __device__ void scan_count_matrix(int32_t *__restrict__ hist_g, int E, int NB,
     }
     __syncthreads();  // the block's writes above are visible to the block
     if (stage != nullptr)
-        for (int i = threadIdx.x; i < n; i += kRankThreads) hist_g[i] = stage[i];
+        for (int i = threadIdx.x; i < n; i += NT) hist_g[i] = stage[i];
     const int total = total_s;
-    for (int e = threadIdx.x; e < E; e += kRankThreads) {
+    for (int e = threadIdx.x; e < E; e += NT) {
         const int b0 = hist[e * NB];
         const int b1 = (e + 1 < E) ? hist[(e + 1) * NB] : total;
         offsets[e] = b0;
@@ -111,19 +120,21 @@ __device__ void scan_count_matrix(int32_t *__restrict__ hist_g, int E, int NB,
 // rank among the chunk's pairs of expert e), or -1 for an expert id outside
 // [0, E), which is reported and dropped.  The ticket must be 0 when the
 // launch starts; the last block leaves it 0.  Dynamic shared memory:
-// max(kRankWarps * E, staged count matrix) ints.
-__global__ void __launch_bounds__(kRankThreads)
+// max(NT / 32 * E, staged count matrix) ints.
+template <int NT>
+__global__ void __launch_bounds__(NT)
 rank_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB, int staged,
             int32_t *__restrict__ hist, int32_t *__restrict__ packed,
             int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
             unsigned *__restrict__ ticket, DevStatus ds) {
     pdl_entry();
-    extern __shared__ int sh_warp[];  // [kRankWarps][E]: per-warp counts, then first ranks
+    constexpr int NW = NT / 32;
+    extern __shared__ int sh_warp[];  // [NW][E]: per-warp counts, then first ranks
     __shared__ int s_last;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kRankWarps * E; i += kRankThreads) sh_warp[i] = 0;
+    for (int i = threadIdx.x; i < NW * E; i += NT) sh_warp[i] = 0;
     __syncthreads();
-    const int sub = (chunk + kRankWarps - 1) / kRankWarps;
+    const int sub = (chunk + NW - 1) / NW;
     const int64_t cend = min((int64_t)(blockIdx.x + 1) * chunk, P);
     const int64_t w0 = min((int64_t)blockIdx.x * chunk + (int64_t)wid * sub, cend);
     const int64_t w1 = min(w0 + sub, cend);
@@ -137,9 +148,9 @@ rank_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB
             raise_error(ds, kErrBadRouting);
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kRankThreads) {
+    for (int e = threadIdx.x; e < E; e += NT) {
         int run = 0;
-        for (int w = 0; w < kRankWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const int c = sh_warp[w * E + e];
             sh_warp[w * E + e] = run;
             run += c;
@@ -174,7 +185,7 @@ rank_kernel(const int32_t *__restrict__ idx, int64_t P, int E, int chunk, int NB
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    scan_count_matrix(hist, E, NB, counts, offsets, staged ? sh_warp : nullptr);
+    scan_count_matrix<NT>(hist, E, NB, counts, offsets, staged ? sh_warp : nullptr);
     if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call (stream order)
 }
 
@@ -241,6 +252,59 @@ place_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist,
     }
 }
 
+// Launch 2 of a standalone dispatch with rows copied unscaled: one warp per
+// token t.  The warp copies x's row t into shared memory (cp.async) before
+// it waits for launch 1, so the read overlaps the ranking.  The read is
+// ordered after every earlier write of x: launch 1 follows the ticket's
+// memset, so it starts only once all earlier work in the stream has
+// completed; this grid starts only once every block of launch 1 has started;
+// and neither launch writes x.  After
+// the wait, lane j looks up pair (t, j)'s row and writes pos and src_token,
+// and the warp writes the staged row to each of the token's rows of x_perm.
+template <typename TA>
+__global__ void __launch_bounds__(32 * kTokWarps)
+place_token_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hist, int64_t T,
+                        int k, int d, int chunk, int NB, int32_t *__restrict__ pos,
+                        int32_t *__restrict__ src_token, TA *__restrict__ x_perm) {
+    extern __shared__ __align__(16) unsigned char stage_raw[];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t t = (int64_t)blockIdx.x * kTokWarps + wid;
+    const int nvec = d * (int)sizeof(TA) / 16;
+    const uint4 *buf = reinterpret_cast<const uint4 *>(stage_raw) + (int64_t)wid * nvec;
+    if (t < T) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d);
+        for (int i = lane; i < nvec; i += 32) tc::cp_async16(tc::smem_u32(buf + i), src + i);
+        tc::cp_async_commit();
+    }
+    pdl_entry();
+    if (t >= T) return;  // warp-uniform
+    bool staged = false;
+    for (int j0 = 0; j0 < k; j0 += 32) {
+        int row = -1;
+        if (j0 + lane < k) {
+            const int64_t q = t * k + j0 + lane;
+            const int v = pos[q];  // (expert << kRankBits) | rank, from launch 1
+            if (v >= 0) {          // else a dropped pair: pos stays -1
+                row = hist[(int64_t)(v >> kRankBits) * NB + (int)(q / chunk)] + (v & kRankMask);
+                pos[q] = row;
+                src_token[row] = (int32_t)t;
+            }
+        }
+        if (!staged) {  // each lane reads back only the vectors it copied
+            tc::cp_async_wait_all();
+            staged = true;
+        }
+        const int nj = min(32, k - j0);
+        for (int jj = 0; jj < nj; ++jj) {
+            const int r = __shfl_sync(0xffffffffu, row, jj);
+            if (r < 0) continue;  // warp-uniform
+            uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d);
+#pragma unroll 4
+            for (int i = lane; i < nvec; i += 32) stg16(dst + i, buf[i]);
+        }
+    }
+}
+
 // Launch 2 when no row moves (x_perm == nullptr: the experts gather the rows
 // themselves): a thread per pair, the same row lookup as place_rows_kernel.
 // With row_scale, also row_scale[row] = w[q] (the weight the experts apply
@@ -292,6 +356,33 @@ dispatch_all_experts_kernel(const int32_t *__restrict__ idx, int64_t T, int E,
     }
 }
 
+// place_token_rows_kernel with up to kTokWarps x 16 KB of shared memory; the
+// carveout favours shared memory, since the kernel uses no L1 caching.
+template <typename TA>
+cudaError_t launch_token_rows(const void *x, const int32_t *hist, const Shape &s,
+                              const DispatchGrid &g, int32_t *pos, int32_t *src_token,
+                              void *x_perm, unsigned blocks, size_t smem, cudaStream_t st) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        if ((err = cudaFuncSetAttribute(place_token_rows_kernel<TA>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kTokWarps * kStageRowMax)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(place_token_rows_kernel<TA>,
+                                        cudaFuncAttributePreferredSharedMemoryCarveout,
+                                        (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+            return err;
+        attr_set[dev] = true;
+    }
+    launch_pdl(place_token_rows_kernel<TA>, dim3(blocks), dim3(32 * kTokWarps), smem, st,
+               static_cast<const TA *>(x), hist, s.T, s.k, s.d, g.chunk, g.blocks, pos, src_token,
+               static_cast<TA *>(x_perm));
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_all_experts(const Shape &s, const int32_t *idx, int32_t *counts,
@@ -338,29 +429,42 @@ unsigned *dispatch_ticket(const Shape &s, int32_t *scratch) {
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
-                            const float *scale, bool ticket_zeroed, float *row_scale) {
+                            const float *scale, bool in_forward, float *row_scale) {
     static bool attr_set[64] = {};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {  // E = 1024: 32 warps x 1024 counts = 128 KB
-        if ((err = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kRankWarps * 1024 * (int)sizeof(int))) != cudaSuccess)
+        if ((err = cudaFuncSetAttribute(rank_kernel<kRankThreads>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kRankWarps * 1024 * (int)sizeof(int))) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(rank_kernel<kSmallRankThreads>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kScanStageMax * (int)sizeof(int))) != cudaSuccess)
             return err;
         attr_set[dev] = true;
     }
     const int64_t P = s.P();
     const DispatchGrid g = dispatch_grid(P, s.E);
     unsigned *ticket = dispatch_ticket(s, hist);
-    if (!ticket_zeroed && (err = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st)) != cudaSuccess)
+    if (!in_forward && (err = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st)) != cudaSuccess)
         return err;
     const int64_t n_hist = (int64_t)s.E * g.blocks;
     const int staged = n_hist <= kScanStageMax ? 1 : 0;
-    const size_t sh = sizeof(int) * (size_t)std::max<int64_t>((int64_t)kRankWarps * s.E,
+    // chunks of 256 pairs: one warp per 32 of them (a block of 1024 threads
+    // would leave most lanes idle, and its per-expert walk over 32 warps'
+    // counts is serial)
+    const bool small = g.chunk == kSmallRankThreads;
+    const int nw = small ? kSmallRankThreads / 32 : kRankWarps;
+    const size_t sh = sizeof(int) * (size_t)std::max<int64_t>((int64_t)nw * s.E,
                                                                staged ? n_hist : 0);
-    launch_pdl(rank_kernel, dim3(g.blocks), dim3(kRankThreads), sh, st, idx, P, s.E, g.chunk,
-               g.blocks, staged, hist, pos, counts, offsets, ticket, ds);
+    if (small)
+        launch_pdl(rank_kernel<kSmallRankThreads>, dim3(g.blocks), dim3(kSmallRankThreads), sh, st,
+                   idx, P, s.E, g.chunk, g.blocks, staged, hist, pos, counts, offsets, ticket, ds);
+    else
+        launch_pdl(rank_kernel<kRankThreads>, dim3(g.blocks), dim3(kRankThreads), sh, st, idx, P,
+                   s.E, g.chunk, g.blocks, staged, hist, pos, counts, offsets, ticket, ds);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (x_perm == nullptr) {  // pos and src_token only (moe_forward's gathered-row path)
         launch_pdl(place_index_kernel, dim3((unsigned)((P + kThreads - 1) / kThreads)),
@@ -370,6 +474,16 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
     }
     const unsigned blocks = (unsigned)((P + kWarps - 1) / kWarps);
     const int32_t *chist = hist;
+    const int64_t row_bytes = (int64_t)s.d * (s.bf16 ? 2 : 4);
+    if (!in_forward && scale == nullptr && row_bytes <= kStageRowMax &&
+        (int64_t)s.k * 1024 <= row_bytes) {
+        const unsigned tblocks = (unsigned)((s.T + kTokWarps - 1) / kTokWarps);
+        const size_t tsh = (size_t)kTokWarps * (size_t)row_bytes;
+        if (s.bf16)
+            return launch_token_rows<__nv_bfloat16>(x, chist, s, g, pos, src_token, x_perm,
+                                                    tblocks, tsh, st);
+        return launch_token_rows<float>(x, chist, s, g, pos, src_token, x_perm, tblocks, tsh, st);
+    }
     if (s.bf16) {
         using T = __nv_bfloat16;
         const T *xt = static_cast<const T *>(x);

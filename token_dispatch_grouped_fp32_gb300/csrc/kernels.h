@@ -64,12 +64,15 @@ unsigned *dispatch_ticket(const Shape &s, int32_t *hist);
 // x_perm == nullptr: counts, offsets, pos and src_token only (no row gather).
 // scale != nullptr: each gathered row is multiplied by its pair's weight;
 // without x_perm, row_scale[row] = scale[pair] instead (if row_scale).
-// ticket_zeroed: an earlier kernel in the stream already cleared the ticket;
-// otherwise it is cleared here with a 4-byte cudaMemsetAsync.
+// in_forward: the dispatch runs inside moe_forward, after the route, whose
+// last launch cleared the ticket; its launches overlap the route's by
+// programmatic dependent launch.  Otherwise (a standalone call) the ticket is
+// cleared here with a 4-byte cudaMemsetAsync, after which the first launch
+// starts only once all earlier work in the stream is done.
 cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, int32_t *counts,
                             int32_t *offsets, int32_t *pos, int32_t *src_token, void *x_perm,
                             int32_t *hist, const DevStatus &ds, cudaStream_t st,
-                            const float *scale = nullptr, bool ticket_zeroed = false,
+                            const float *scale = nullptr, bool in_forward = false,
                             float *row_scale = nullptr);
 
 // Grouped SwiGLU experts.  bf16: tcgen05 tensor-core path; fp32: SIMT path.

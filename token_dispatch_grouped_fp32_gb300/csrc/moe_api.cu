@@ -510,7 +510,7 @@ moe_status_t moe_forward(const moe_config_t *cfg, const void *x, const float *Wr
     else
         st = from_cuda(launch_dispatch(s, idx, x, counts, offsets, pos, src,
                                        gather ? nullptr : x_perm, hist, ds, cs,
-                                       s.scale_inputs ? w : nullptr, /*ticket_zeroed=*/true,
+                                       s.scale_inputs ? w : nullptr, /*in_forward=*/true,
                                        row_scale),
                        "dispatch launch");
     if (st != MOE_OK) return st;
