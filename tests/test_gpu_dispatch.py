@@ -57,6 +57,14 @@ DISPATCH_CASES = [
     (4000, 16, 2, 8, torch.bfloat16, 50.0),    # one expert takes every token
     (6000, 1024, 8, 8, torch.bfloat16, 0.0),   # many experts, most empty per chunk
     (300000, 16, 8, 8, torch.bfloat16, 0.0),   # 2.4M pairs: chunks grow past 2048
+    # rows of at least k KB and at most 16 KB: a warp per token stages its row
+    # in shared memory before the ranking ends and writes it k times
+    (700, 8, 2, 1024, torch.bfloat16, 0.0),    # 2 KB rows, 175 blocks of 4 tokens
+    (301, 64, 1, 512, torch.bfloat16, 0.0),    # k = 1 at 1 KB, last block of 1 token
+    (513, 16, 4, 4096, torch.float32, 0.0),    # 16 KB fp32 rows (the largest staged)
+    (257, 8, 2, 8192, torch.bfloat16, 50.0),   # 16 KB bf16 rows, one expert takes most
+    (130, 8, 2, 8200, torch.bfloat16, 0.0),    # 16,400-byte rows: a warp per pair again
+    (64, 32, 8, 2048, torch.bfloat16, 0.0),    # 4 KB rows with k = 8: a warp per pair
 ]
 
 
@@ -75,17 +83,24 @@ def test_dispatch_matches_oracle(moe, oracle, T, E, k, d, dtype, skew):
     assert torch.equal(x_perm, x[torch.from_numpy(rs).long()])
 
 
-@pytest.mark.parametrize("T", [50, 20000])  # one chunk / 157 chunks of 256
-def test_dispatch_flags_out_of_range_expert(moe, oracle, T):
+@pytest.mark.parametrize("T,d", [(50, 16), (20000, 16), (50, 2048)])  # one chunk / 157
+def test_dispatch_flags_out_of_range_expert(moe, oracle, T, d):    # chunks / rows staged
     E, k = 8, 2
     idx = _routing(oracle, T, E, k, 5)
     idx[7, 1] = E + 3
-    x = torch.randn(T, 16).to(torch.bfloat16)
+    x = torch.randn(T, d).to(torch.bfloat16)
     moe.moe_last_device_error(raise_on_error=False)  # clear
-    counts, offsets, pos, src, _ = _run_dispatch(moe, idx, x, E)
+    counts, offsets, pos, src, x_perm = _run_dispatch(moe, idx, x, E)
     assert moe.moe_last_device_error(raise_on_error=False) == moe.MOE_ERR_BAD_ROUTING
     assert counts.sum() == T * k - 1 and offsets[-1] == T * k - 1
     assert pos[7 * k + 1] == -1
+    # every placed row is its token's row; the dropped pair's token still has
+    # its other pair placed
+    keep = pos >= 0
+    rows = torch.from_numpy(pos[keep]).long()
+    toks = torch.from_numpy(np.nonzero(keep)[0] // k).long()
+    assert torch.equal(x_perm[rows], x[toks])
+    assert x_perm.shape[0] == T * k and int(keep.sum()) == T * k - 1
     assert moe.moe_last_device_error(raise_on_error=False) == moe.MOE_OK  # cleared
 
 
