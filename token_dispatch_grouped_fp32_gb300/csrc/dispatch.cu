@@ -17,8 +17,8 @@
 // offsets, and resets the ticket for the next call.
 // Launch 2 (place_rows_kernel), one warp per pair: row = first row of the
 // pair's (expert, chunk) + its rank; writes pos, src_token and copies the
-// token's row into x_perm.  A standalone dispatch with unscaled rows of at
-// most 16 KB uses place_token_rows_kernel instead, a warp per token, which
+// token's row into x_perm.  A standalone dispatch with unscaled rows of k KB
+// to 16 KB uses place_token_rows_kernel instead, a warp per token, which
 // reads the token's row while launch 1 still runs.  Without x_perm (the
 // experts gather the rows), place_index_kernel does the lookup alone, a
 // thread per pair.
@@ -37,9 +37,9 @@ constexpr int kThreads = 256;      // place_rows_kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kTokWarps = 4;              // place_token_rows_kernel: tokens per block
 constexpr int kStageRowMax = 16 * 1024;   // its largest row, staged in shared memory
-constexpr int kRankThreads = 1024;  // rank_kernel (256 for chunks of 256 pairs)
+constexpr int kRankThreads = 1024;  // rank_kernel for chunks of 2048 pairs and more
 constexpr int kRankWarps = kRankThreads / 32;
-constexpr int kSmallRankThreads = 256;
+constexpr int kSmallRankThreads = 256;  // rank_kernel for chunks of 256 pairs
 // The count matrix is staged in shared memory for the scan when it has at
 // most this many entries (else the scan reads it through L2).
 constexpr int kScanStageMax = 16 * 1024;
