@@ -131,3 +131,71 @@ def test_dispatch_scales_rows_when_weights_act_on_inputs(moe, oracle, dtype):
     expect = (x.float()[torch.from_numpy(rs).long()] *
               wt.reshape(-1)[torch.from_numpy(pair_of_row)][:, None]).to(dtype)
     assert torch.equal(x_perm.cpu(), expect)
+
+
+def test_dispatch_reads_x_written_just_before(moe, oracle):
+    """The row copy of a standalone dispatch reads x before it waits for the
+    ranking; x written by the kernel just before the call, on the same
+    stream, must still be what it copies.  Each round overwrites x on the
+    device and dispatches at once; every row of x_perm is checked."""
+    T, E, k, d = 700, 8, 2, 1024  # rows staged per token (2 KB, k = 2)
+    idx = _routing(oracle, T, E, k, 19)
+    _, _, _, rs = oracle.dispatch(idx, E)
+    cfg = moe.config(T, d, E, k, 8, torch.bfloat16)
+    P = T * k
+    dev = "cuda"
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    pos = torch.empty(P, dtype=torch.int32, device=dev)
+    src = torch.empty(P, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(P, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device=dev)
+    idx_d = torch.from_numpy(idx).cuda()
+    x_d = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    g = torch.Generator(device=dev).manual_seed(5)
+    for _ in range(4):
+        x_d.normal_(generator=g)  # a kernel writing x just before the dispatch
+        moe.moe_dispatch(cfg, idx_d, None, x_d, counts, offsets, pos, src, x_perm, ws)
+        assert torch.equal(x_perm, x_d[torch.from_numpy(rs).long().cuda()])
+
+
+def test_dispatch_in_a_cuda_graph(moe, oracle):
+    """A standalone dispatch captured in a CUDA graph (its memset, the rank
+    launch and the row copy) and replayed on new routing and rows gives the
+    oracle's result each time."""
+    T, E, k, d = 513, 8, 2, 2048
+    cfg = moe.config(T, d, E, k, 8, torch.bfloat16)
+    P = T * k
+    dev = "cuda"
+    idx_d = torch.empty(T, k, dtype=torch.int32, device=dev)
+    x_d = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    pos = torch.empty(P, dtype=torch.int32, device=dev)
+    src = torch.empty(P, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(P, d, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(256, moe.moe_dispatch_workspace_size(cfg)), dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream()
+    idx0 = _routing(oracle, T, E, k, 1)
+    idx_d.copy_(torch.from_numpy(idx0))
+    x_d.normal_()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):  # one eager call first: the library's set-up
+        moe.moe_dispatch(cfg, idx_d, None, x_d, counts, offsets, pos, src, x_perm, ws, stream=st)
+    st.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=st):
+        moe.moe_dispatch(cfg, idx_d, None, x_d, counts, offsets, pos, src, x_perm, ws, stream=st)
+    for seed in (2, 3):
+        idx = _routing(oracle, T, E, k, seed)
+        idx_d.copy_(torch.from_numpy(idx))
+        x = torch.randn(T, d, generator=torch.Generator().manual_seed(seed)).to(torch.bfloat16)
+        x_d.copy_(x)
+        graph.replay()
+        torch.cuda.synchronize()
+        rc, ro, rp, rs = oracle.dispatch(idx, E)
+        np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+        np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+        np.testing.assert_array_equal(pos.cpu().numpy(), rp)
+        np.testing.assert_array_equal(src.cpu().numpy(), rs)
+        assert torch.equal(x_perm.cpu(), x[torch.from_numpy(rs).long()])
