@@ -136,7 +136,8 @@ size_t moe_dispatch_workspace_size(const moe_config_t *cfg);
 /*
  * Number of kernel launches one moe_forward call makes for `cfg`: the router
  * (1 to 3 launches, by path), the dispatch (2; 1 when k == E, except for
- * fp32 with scale_inputs), the two grouped GEMMs (2, or
+ * fp32 with scale_inputs, and 1 when it copies unscaled rows with E <= 16
+ * and P <= 16384 as described at moe_dispatch), the two grouped GEMMs (2, or
  * 4 when bf16 experts average 64 to 511 rows each and are split between two
  * tile shapes) and the combine (1).  0 when T == 0; -1 for an invalid
  * configuration.  Makes no CUDA call.
@@ -205,6 +206,10 @@ moe_status_t moe_route_from_logits(const moe_config_t *cfg, const float *logits,
  * last block, the scan that yields counts and offsets) and a kernel that
  * places every pair's row and copies it.  The rank kernel's ticket counter
  * in ws is cleared first with a 4-byte cudaMemsetAsync on `stream`.
+ * One launch, with ws not touched and no memset, when E <= 16, P <= 16384,
+ * the rows are not scaled and a row is k KB to 16 KB (d * element size):
+ * every block of that launch counts all P ids itself and places its own
+ * tokens' pairs.
  */
 moe_status_t moe_dispatch(const moe_config_t *cfg, const int32_t *topk_idx,
                           const float *topk_w, const void *x, int32_t *counts,

@@ -155,8 +155,20 @@ def test_input_scaling_needs_weights_at_dispatch_only(moe):
 def test_forward_kernel_launches(moe):
     """The bench's gpu_launches claim comes from the library's own launch plan."""
     # Mixtral-shaped, bf16, E = 8, T = 4096: tensor-core router (weight split,
-    # logits, top-k) + dispatch (rank, place rows) + G1, G2 + combine
-    assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 8
+    # logits, top-k) + dispatch (one launch: E <= 16, P <= 16384, 8 KB rows)
+    # + G1, G2 + combine
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "bf16")) == 7
+    # the dispatch in two launches (rank, place rows): P > 16384, E > 16,
+    # rows under k KB, or rows scaled by the weights (fp32 copies them)
+    assert moe.moe_forward_kernel_launches(moe.config(8193, 4096, 16, 2, 14336, "bf16")) == 8
+    # (E = 17: CUDA-core logits with the selection in the same launch)
+    assert moe.moe_forward_kernel_launches(moe.config(8192, 4096, 17, 2, 14336, "bf16")) == 6
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 512, 8, 2, 14336, "bf16")) == 8
+    # fp32 (CUDA-core logits and selection in one launch): 5, and 6 when the
+    # dispatch copies rows scaled by the weights
+    assert moe.moe_forward_kernel_launches(moe.config(4096, 4096, 8, 2, 14336, "f32")) == 5
+    assert moe.moe_forward_kernel_launches(
+        moe.config(4096, 4096, 8, 2, 14336, "f32", scale_inputs=True)) == 6
     # about 256 rows per expert: G1 and G2 each as a CTA-pair launch and a
     # single-CTA launch, the experts split between them
     assert moe.moe_forward_kernel_launches(moe.config(8192, 2880, 128, 4, 2880, "bf16")) == 10

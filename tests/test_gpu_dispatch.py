@@ -65,6 +65,22 @@ DISPATCH_CASES = [
     (257, 8, 2, 8192, torch.bfloat16, 50.0),   # 16 KB bf16 rows, one expert takes most
     (130, 8, 2, 8200, torch.bfloat16, 0.0),    # 16,400-byte rows: a warp per pair again
     (64, 32, 8, 2048, torch.bfloat16, 0.0),    # 4 KB rows with k = 8: a warp per pair
+    # E <= 16 and P <= 16384 with staged rows: one launch, each block counting
+    # every id itself (the cases above with E <= 16 and rows of k KB to 16 KB
+    # take it too)
+    (4096, 8, 2, 4096, torch.bfloat16, 0.0),   # the Mixtral layer's shape: 152 blocks
+    (4096, 8, 2, 4096, torch.float32, 0.0),    # 16 KB fp32 rows: 8 warps a block
+    (4096, 8, 2, 4096, torch.bfloat16, 50.0),  # one expert takes every token
+    (8192, 16, 2, 4096, torch.bfloat16, 0.0),  # P = 16384, the largest; experts 8-15
+    (8193, 16, 2, 4096, torch.bfloat16, 0.0),  # P = 16386: two launches again
+    (2047, 16, 8, 8192, torch.bfloat16, 0.0),  # k = 8, 16 KB rows, ragged blocks
+    (5, 16, 16, 8192, torch.bfloat16, 0.0),    # k = E = 16, one block of 5 tokens
+    (2433, 8, 2, 1024, torch.bfloat16, 0.0),   # just past 152 blocks of 16 tokens
+    (1000, 3, 2, 2048, torch.bfloat16, 0.0),   # three experts
+    (1, 8, 2, 4096, torch.bfloat16, 0.0),      # a single token
+    (64, 8, 2, 4096, torch.bfloat16, 0.0),     # 64 blocks of one token and one warp
+    (1024, 8, 8, 4096, torch.bfloat16, 0.0),   # k = E = 8: each row written 8 times
+    (16384, 16, 1, 1024, torch.bfloat16, 0.0), # k = 1 at P = 16384: 108 tokens a block
 ]
 
 
@@ -83,9 +99,13 @@ def test_dispatch_matches_oracle(moe, oracle, T, E, k, d, dtype, skew):
     assert torch.equal(x_perm, x[torch.from_numpy(rs).long()])
 
 
-@pytest.mark.parametrize("T,d", [(50, 16), (20000, 16), (50, 2048)])  # one chunk / 157
-def test_dispatch_flags_out_of_range_expert(moe, oracle, T, d):    # chunks / rows staged
-    E, k = 8, 2
+@pytest.mark.parametrize("T,d,E", [(50, 16, 8),     # one chunk
+                                   (20000, 16, 8),  # 157 chunks
+                                   (50, 2048, 32),  # rows staged, two launches
+                                   (50, 2048, 8),   # one launch
+                                   (3000, 4096, 8)])  # one launch, many blocks
+def test_dispatch_flags_out_of_range_expert(moe, oracle, T, d, E):
+    k = 2
     idx = _routing(oracle, T, E, k, 5)
     idx[7, 1] = E + 3
     x = torch.randn(T, d).to(torch.bfloat16)
@@ -133,12 +153,13 @@ def test_dispatch_scales_rows_when_weights_act_on_inputs(moe, oracle, dtype):
     assert torch.equal(x_perm.cpu(), expect)
 
 
-def test_dispatch_reads_x_written_just_before(moe, oracle):
-    """The row copy of a standalone dispatch reads x before it waits for the
-    ranking; x written by the kernel just before the call, on the same
-    stream, must still be what it copies.  Each round overwrites x on the
-    device and dispatches at once; every row of x_perm is checked."""
-    T, E, k, d = 700, 8, 2, 1024  # rows staged per token (2 KB, k = 2)
+@pytest.mark.parametrize("E", [8, 32])  # one launch / two launches
+def test_dispatch_reads_x_written_just_before(moe, oracle, E):
+    """The row copy of a standalone dispatch reads x before the ranking is
+    done; x written by the kernel just before the call, on the same stream,
+    must still be what it copies.  Each round overwrites x on the device and
+    dispatches at once; every row of x_perm is checked."""
+    T, k, d = 700, 2, 1024  # rows staged per token (2 KB, k = 2)
     idx = _routing(oracle, T, E, k, 19)
     _, _, _, rs = oracle.dispatch(idx, E)
     cfg = moe.config(T, d, E, k, 8, torch.bfloat16)
@@ -159,11 +180,12 @@ def test_dispatch_reads_x_written_just_before(moe, oracle):
         assert torch.equal(x_perm, x_d[torch.from_numpy(rs).long().cuda()])
 
 
-def test_dispatch_in_a_cuda_graph(moe, oracle):
-    """A standalone dispatch captured in a CUDA graph (its memset, the rank
-    launch and the row copy) and replayed on new routing and rows gives the
-    oracle's result each time."""
-    T, E, k, d = 513, 8, 2, 2048
+@pytest.mark.parametrize("E", [8, 32])
+def test_dispatch_in_a_cuda_graph(moe, oracle, E):
+    """A standalone dispatch captured in a CUDA graph (E = 8: its one launch;
+    E = 32: its memset, the rank launch and the row copy) and replayed on new
+    routing and rows gives the oracle's result each time."""
+    T, k, d = 513, 2, 2048
     cfg = moe.config(T, d, E, k, 8, torch.bfloat16)
     P = T * k
     dev = "cuda"

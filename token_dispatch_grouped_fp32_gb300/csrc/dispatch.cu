@@ -1,6 +1,6 @@
 // dispatch.cu -- token dispatch on one device: per-expert histogram, exclusive
 // scan, stable scatter into expert-contiguous order, and the row gather, in
-// two launches.
+// two launches (one for a standalone dispatch of few experts and pairs).
 //
 // Transformers docs "Expert parallelism", section "Token dispatch": every
 // (token, expert) pair is sent to its expert and the experts run on the rows
@@ -21,7 +21,9 @@
 // to 16 KB uses place_token_rows_kernel instead, a warp per token, which
 // reads the token's row while launch 1 still runs.  Without x_perm (the
 // experts gather the rows), place_index_kernel does the lookup alone, a
-// thread per pair.
+// thread per pair.  A dispatch with E <= 16 and P <= 16384 that copies
+// unscaled rows of k KB to 16 KB runs as one launch instead,
+// dispatch_one_launch_kernel, whose blocks each count every id.
 // Stability: rows of one expert are in ascending pair id, hence ascending
 // token id, and no atomic decides any order.
 #include <algorithm>
@@ -305,6 +307,186 @@ place_token_rows_kernel(const TA *__restrict__ x, const int32_t *__restrict__ hi
     }
 }
 
+// A dispatch with few experts and few pairs in ONE launch (the limits
+// below; rows unscaled, of k KB to 16 KB).  Block b owns the contiguous
+// tokens [b*T/G, (b+1)*T/G) of a grid of G = min(SMs, T) blocks, one warp
+// per token (up to 32 warps; a warp takes a further token each round when
+// the block owns more tokens than its warps).  Each warp first copies its
+// token row into shared memory with cp.async, so the reads of all the
+// block's rows (27 rows of 8 KB each on the Mixtral layer's shape) overlap
+// the ranking.  Every block then reads all P expert ids (at most 64 KB, L2
+// hits after the first block) and counts them per expert in two parts: the
+// pairs before its first pair, and the rest.  The totals give counts and
+// offsets; the first part gives the row at which the block's pairs of each
+// expert start.  So no block waits for another, and no count matrix or
+// ticket is needed.  Per-thread counts are 8-bit fields of two 64-bit words
+// (experts 0-7 and 8-15); the launcher checks that no thread sees more than
+// 255 ids.  The block's pairs are then ranked in pair order (a warp's 32
+// pairs with __match_any_sync, after the warps before it, as rank_kernel
+// does) and each staged row is written to its k rows.
+// Standalone (STAGE_FIRST), the launch carries no programmatic-serialisation
+// attribute, so it starts only after all earlier work in the stream has
+// completed (x and the ids included), and the rows are staged at once; its
+// pdl_entry() then only lets a following kernel be scheduled.  Inside
+// moe_forward it is launched like the layer's other kernels and stages
+// nothing before its wait (x may be the output of a kernel still running).
+constexpr int kOneMaxE = 16;
+constexpr int kOneMaxP = 16384;
+constexpr int kOneMaxWarps = 32;            // per block: a warp per token
+constexpr int kOneStageBytes = 216 * 1024;  // staged rows per block
+constexpr int kOneBlockPairs = 1024;        // pairs one block may own
+
+template <typename TA, bool STAGE_FIRST>
+__global__ void __launch_bounds__(32 * kOneMaxWarps)
+dispatch_one_launch_kernel(const int32_t *__restrict__ idx, const TA *__restrict__ x, int64_t T,
+                           int k, int E, int d, int32_t *__restrict__ counts,
+                           int32_t *__restrict__ offsets, int32_t *__restrict__ pos,
+                           int32_t *__restrict__ src_token, TA *__restrict__ x_perm,
+                           DevStatus ds) {
+    extern __shared__ __align__(16) unsigned char stage_raw[];
+    __shared__ int s_part[kOneMaxWarps][kOneMaxE];  // per-warp counts (before, then rank bases)
+    __shared__ int s_all[kOneMaxWarps][kOneMaxE];   // per-warp counts of all pairs
+    __shared__ int s_base[kOneMaxE];                // next row of each expert in this block
+    __shared__ int s_pair[kOneBlockPairs];          // the block's expert ids, then their rows
+    const int nthr = blockDim.x, nw = nthr >> 5;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * T / gridDim.x;
+    const int64_t t1 = (int64_t)(blockIdx.x + 1) * T / gridDim.x;
+    const int64_t P = T * k, p0 = t0 * k, p1 = t1 * k;
+    const int nvec = d * (int)sizeof(TA) / 16;
+    uint4 *buf = reinterpret_cast<uint4 *>(stage_raw) + (int64_t)wid * nvec;
+    auto stage = [&](int64_t t) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + t * d);
+        for (int i = lane; i < nvec; i += 32) tc::cp_async16(tc::smem_u32(buf + i), src + i);
+        tc::cp_async_commit();
+    };
+    if (STAGE_FIRST && t0 + wid < t1) stage(t0 + wid);
+    pdl_entry();
+    if (!STAGE_FIRST && t0 + wid < t1) stage(t0 + wid);
+
+    // 8-bit field e & 7 of word lo (e < 8) or hi (8 <= e < 16); other ids add 0
+    auto field = [E](int e) -> uint64_t {
+        return (unsigned)e < (unsigned)E ? 1ull << ((e & 7) << 3) : 0ull;
+    };
+    uint64_t pre_lo = 0, pre_hi = 0, rest_lo = 0, rest_hi = 0;
+    auto tally = [&](int64_t i, int e) {
+        const uint64_t inc = field(e);
+        const uint64_t lo = e < 8 ? inc : 0ull, hi = e < 8 ? 0ull : inc;
+        if (i < p0) {
+            pre_lo += lo;
+            pre_hi += hi;
+        } else {
+            rest_lo += lo;
+            rest_hi += hi;
+            if (i < p1) s_pair[i - p0] = e;  // the block's own pairs, for the ranking
+        }
+    };
+    int64_t scalar_from = 0;
+    if ((reinterpret_cast<uintptr_t>(idx) & 15u) == 0) {  // 16-byte loads of four ids
+        const int64_t nv = P >> 2;
+        const int4 *v4 = reinterpret_cast<const int4 *>(idx);
+#pragma unroll 4
+        for (int64_t v = threadIdx.x; v < nv; v += nthr) {
+            const int4 e4 = v4[v];
+            tally(4 * v, e4.x);
+            tally(4 * v + 1, e4.y);
+            tally(4 * v + 2, e4.z);
+            tally(4 * v + 3, e4.w);
+        }
+        scalar_from = nv << 2;
+    }
+    for (int64_t i = scalar_from + threadIdx.x; i < P; i += nthr) tally(i, idx[i]);
+    for (int e = 0; e < E; ++e) {
+        const int sh = (e & 7) << 3;
+        const unsigned pv = (unsigned)(((e < 8 ? pre_lo : pre_hi) >> sh) & 255u);
+        const unsigned rv = (unsigned)(((e < 8 ? rest_lo : rest_hi) >> sh) & 255u);
+        const int ps = (int)__reduce_add_sync(0xffffffffu, pv);
+        const int rs = (int)__reduce_add_sync(0xffffffffu, rv);
+        if (lane == 0) {
+            s_part[wid][e] = ps;
+            s_all[wid][e] = ps + rs;
+        }
+    }
+    __syncthreads();
+    if (wid == 0) {  // lane e: expert e's total, its offset and the block's first row
+        int tot = 0, pre = 0;
+        if (lane < E)
+            for (int w = 0; w < nw; ++w) {
+                tot += s_all[w][lane];
+                pre += s_part[w][lane];
+            }
+        int incl = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        const int total = __shfl_sync(0xffffffffu, incl, 31);  // lanes >= E add 0
+        if (lane < E) s_base[lane] = incl - tot + pre;
+        if (blockIdx.x == 0) {
+            if (lane < E) {
+                counts[lane] = tot;
+                offsets[lane] = incl - tot;
+            }
+            if (lane == 0) offsets[E] = total;
+        }
+    }
+    __syncthreads();
+
+    // Rank the block's pairs [p0, p1) in pair order, nthr at a time.
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int64_t qb = p0; qb < p1; qb += nthr) {
+        const int64_t q = qb + threadIdx.x;
+        int e = -1;
+        if (q < p1) {
+            e = s_pair[q - p0];
+            if ((unsigned)e >= (unsigned)E) {
+                raise_error(ds, kErrBadRouting);  // the pair is dropped
+                e = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int before = __popc(peers & lt_mask);
+        if (lane < E) s_part[wid][lane] = 0;
+        __syncwarp();
+        if (e >= 0 && lane == 31 - __clz(peers)) s_part[wid][e] = __popc(peers);
+        __syncthreads();
+        if (threadIdx.x < E) {  // per expert: the warps' bases, in warp order
+            int run = s_base[threadIdx.x];
+            for (int w = 0; w < nw; ++w) {
+                const int c = s_part[w][threadIdx.x];
+                s_part[w][threadIdx.x] = run;
+                run += c;
+            }
+            s_base[threadIdx.x] = run;
+        }
+        __syncthreads();
+        if (q < p1) {
+            const int row = e >= 0 ? s_part[wid][e] + before : -1;
+            s_pair[q - p0] = row;  // this thread alone read that entry
+            pos[q] = row;
+            if (row >= 0) src_token[row] = (int32_t)(q / k);
+        }
+        __syncthreads();  // the rows are complete; s_part may be reused
+    }
+
+    // Each warp writes its staged token rows to their k rows of x_perm.  A
+    // lane reads back only the vectors it staged, so the next token's
+    // cp.async into the same buffer follows that lane's own reads.
+    for (int64_t t = t0 + wid; t < t1; t += nw) {
+        if (t != t0 + wid) stage(t);
+        tc::cp_async_wait_all();
+        const int b = (int)((t - t0) * k);
+        for (int j = 0; j < k; ++j) {
+            const int r = s_pair[b + j];
+            if (r < 0) continue;  // warp-uniform: a dropped pair
+            uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d);
+#pragma unroll 4
+            for (int i = lane; i < nvec; i += 32) stg16(dst + i, buf[i]);
+        }
+    }
+}
+
 // Launch 2 when no row moves (x_perm == nullptr: the experts gather the rows
 // themselves): a thread per pair, the same row lookup as place_rows_kernel.
 // With row_scale, also row_scale[row] = w[q] (the weight the experts apply
@@ -383,7 +565,64 @@ cudaError_t launch_token_rows(const void *x, const int32_t *hist, const Shape &s
     return cudaGetLastError();
 }
 
+// dispatch_one_launch_kernel where dispatch_fits_one_launch(s), the block
+// count leaves at most kOneBlockPairs pairs per block and no thread counts
+// more than 255 ids (both hold on a GPU of up to 1024 SMs).  *launched says
+// whether it launched; otherwise it returns cudaSuccess.
+template <typename TA>
+cudaError_t launch_dispatch_one(const Shape &s, const int32_t *idx, const void *x,
+                                int32_t *counts, int32_t *offsets, int32_t *pos,
+                                int32_t *src_token, void *x_perm, const DevStatus &ds,
+                                cudaStream_t st, bool in_forward, bool *launched) {
+    *launched = false;
+    static bool attr_set[64] = {};
+    static int sms[64] = {};
+    const int64_t row_bytes = (int64_t)s.d * (int64_t)sizeof(TA);
+    if (!dispatch_fits_one_launch(s)) return cudaSuccess;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        if ((err = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) !=
+                cudaSuccess ||
+            (err = cudaFuncSetAttribute(dispatch_one_launch_kernel<TA, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kOneStageBytes)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(dispatch_one_launch_kernel<TA, false>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kOneStageBytes)) != cudaSuccess)
+            return err;
+        attr_set[dev] = true;
+    }
+    const int64_t P = s.P();
+    const int64_t blocks = std::min<int64_t>(sms[dev], s.T);
+    const int64_t tok = (s.T + blocks - 1) / blocks;  // most tokens a block owns
+    const int nw = (int)std::min<int64_t>(std::min<int64_t>(kOneMaxWarps, tok),
+                                          kOneStageBytes / row_bytes);
+    const int64_t nthr = 32 * (int64_t)nw;
+    if (blocks < 1 || tok * s.k > kOneBlockPairs || (P + nthr - 1) / nthr + 5 > 255)
+        return cudaSuccess;
+    *launched = true;
+    const size_t smem = (size_t)nw * (size_t)row_bytes;
+    if (in_forward)
+        launch_pdl(dispatch_one_launch_kernel<TA, false>, dim3((unsigned)blocks), dim3(32 * nw),
+                   smem, st, idx, static_cast<const TA *>(x), s.T, s.k, s.E, s.d, counts,
+                   offsets, pos, src_token, static_cast<TA *>(x_perm), ds);
+    else
+        dispatch_one_launch_kernel<TA, true><<<(unsigned)blocks, 32 * nw, smem, st>>>(
+            idx, static_cast<const TA *>(x), s.T, s.k, s.E, s.d, counts, offsets, pos, src_token,
+            static_cast<TA *>(x_perm), ds);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+bool dispatch_fits_one_launch(const Shape &s) {
+    const int64_t row_bytes = (int64_t)s.d * (s.bf16 ? 2 : 4);
+    return s.E <= kOneMaxE && s.P() <= kOneMaxP && row_bytes <= kStageRowMax &&
+           (int64_t)s.k * 1024 <= row_bytes;
+}
 
 cudaError_t launch_dispatch_all_experts(const Shape &s, const int32_t *idx, int32_t *counts,
                                         int32_t *offsets, int32_t *pos, int32_t *src_token,
@@ -446,6 +685,15 @@ cudaError_t launch_dispatch(const Shape &s, const int32_t *idx, const void *x, i
         attr_set[dev] = true;
     }
     const int64_t P = s.P();
+    if (scale == nullptr && x_perm != nullptr) {
+        bool one = false;
+        err = s.bf16 ? launch_dispatch_one<__nv_bfloat16>(s, idx, x, counts, offsets, pos,
+                                                          src_token, x_perm, ds, st, in_forward,
+                                                          &one)
+                     : launch_dispatch_one<float>(s, idx, x, counts, offsets, pos, src_token,
+                                                  x_perm, ds, st, in_forward, &one);
+        if (err != cudaSuccess || one) return err;
+    }
     const DispatchGrid g = dispatch_grid(P, s.E);
     unsigned *ticket = dispatch_ticket(s, hist);
     if (!in_forward && (err = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st)) != cudaSuccess)

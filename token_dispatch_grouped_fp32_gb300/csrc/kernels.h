@@ -57,6 +57,9 @@ struct DispatchGrid {
     int blocks;  // number of blocks (>= 1 when P > 0)
 };
 DispatchGrid dispatch_grid(int64_t P, int E);
+// A dispatch that copies unscaled rows runs as one launch (no count matrix,
+// no ticket) when E <= 16, P <= 16384 and a row is k KB to 16 KB.
+bool dispatch_fits_one_launch(const Shape &s);
 size_t dispatch_scratch_bytes(const Shape &s);  // count matrix [E][chunks] + ticket
 // The ticket counter inside the dispatch scratch `hist` (must be 0 when the
 // dispatch's first launch starts; the dispatch leaves it 0).

@@ -354,7 +354,12 @@ int moe_forward_kernel_launches(const moe_config_t *cfg) {
     // CUDA cores selecting in the logits launch, or CUDA-core logits + top-k
     const int route = router_tc_eligible(s) ? 3 : router_selects_in_logits(s) ? 1 : 2;
     const int experts = s.bf16 ? grouped_swiglu_tc_launches(s) : 2 /* G1, G2 */;
-    const int dispatch = all_experts_path(s) ? 1 : 2;  // rank (with the count scan), place rows
+    // rank (with the count scan) and place rows, or one launch for few experts and pairs
+    const int dispatch = all_experts_path(s) ||
+                                 (forward_uses_x_perm(s) && !s.scale_inputs &&
+                                  dispatch_fits_one_launch(s))
+                             ? 1
+                             : 2;
     return route + dispatch + experts + 1 /* combine */;
 }
 
