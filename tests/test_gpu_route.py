@@ -104,6 +104,8 @@ def test_route_logits_and_selection(moe, oracle, name, T):
 TC_SHAPES = [
     # T, d, E, k
     (1024, 256, 8, 2),
+    (1024, 4160, 8, 2),     # E = 8, d = 65 K steps
+    (16400, 256, 8, 2),     # E = 8, 129 token tiles (the last of 16 tokens)
     (1100, 512, 24, 3),
     (2000, 128, 40, 4),
     (1500, 320, 48, 6),
@@ -132,6 +134,7 @@ SIMT_SHAPES = [
     (2048, 64, 520, 8, "bf16"),    # E > 256: tiled kernel, ragged column tile
     (1000, 320, 100, 5, "f32"),    # T < 2048: 32-expert groups, top-k launch
     (777, 96, 24, 3, "f32"),       # E <= 32: selection in the logits launch
+    (1024, 264, 8, 2, "bf16"),     # E = 8 with d % 64 != 0: the same
 ]
 
 

@@ -69,6 +69,54 @@ __device__ __forceinline__ bool ranks_before(float a, int ia, float b, int ib) {
     return ia < ib;
 }
 
+// Top-k selection and softmax weights inside EP-lane segments of a warp:
+// lane tt*EP + e holds the logit v of expert e of the segment's token
+// (valid: e is one of its experts).  Every lane of the warp must call it.
+// Slot j of the token's selection ends in lane tt*EP + j, which stores it
+// to idx_row[j] and w_row[j] when `store`.
+template <int EP>
+__device__ __forceinline__ void select_in_segment(float v, int e, bool valid, int k, int renorm,
+                                                  bool store, int32_t *idx_row, float *w_row) {
+    bool avail = valid;
+    float my_v = 0.f;
+    int my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = avail ? v : NAN;
+        int be = avail ? e : kNoExpert;
+#pragma unroll
+        for (int off = EP / 2; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (oe != kNoExpert && (be == kNoExpert || ranks_before(ov, oe, bv, be))) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be == e) avail = false;
+        if (e == j) {
+            my_v = bv;
+            my_e = be;
+        }
+    }
+    float m = valid ? v : -INFINITY;
+#pragma unroll
+    for (int off = EP / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float z = valid ? expf(v - m) : 0.f;
+#pragma unroll
+    for (int off = EP / 2; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    float pr = (e < k) ? expf(my_v - m) / z : 0.f;
+    if (renorm) {
+        float sum = pr;
+#pragma unroll
+        for (int off = EP / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        pr = pr / sum;
+    }
+    if (e < k && store) {
+        idx_row[e] = my_e;
+        w_row[e] = pr;
+    }
+}
+
 template <typename TA, int EP>
 __global__ void __launch_bounds__(256)
 router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ Wr,
@@ -146,45 +194,9 @@ router_logits_split_kernel(const TA *__restrict__ x, const float *__restrict__ W
         // E <= 32: select and weigh here, on exactly the values just written.
         // Token tt's logits sit in the EP-lane segment of lanes tt*EP + e.
         if (topk_idx != nullptr) {  // warp-uniform: every lane joins the shuffles
-            const bool valid = e < ne;
-            bool avail = valid;
-            float my_v = 0.f;
-            int my_e = 0;
-            for (int j = 0; j < k; ++j) {
-                float bv = avail ? v : NAN;
-                int be = avail ? e : kNoExpert;
-#pragma unroll
-                for (int off = EP / 2; off > 0; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                    const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                    if (oe != kNoExpert && (be == kNoExpert || ranks_before(ov, oe, bv, be))) {
-                        bv = ov;
-                        be = oe;
-                    }
-                }
-                if (be == e) avail = false;
-                if (e == j) {
-                    my_v = bv;
-                    my_e = be;
-                }
-            }
-            float m = valid ? v : -INFINITY;
-#pragma unroll
-            for (int off = EP / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            float z = valid ? expf(v - m) : 0.f;
-#pragma unroll
-            for (int off = EP / 2; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-            float pr = (e < k) ? expf(my_v - m) / z : 0.f;
-            if (renorm) {
-                float sum = pr;
-#pragma unroll
-                for (int off = EP / 2; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                pr = pr / sum;
-            }
-            if (e < k && t < T) {
-                topk_idx[t * k + e] = my_e;
-                topk_w[t * k + e] = pr;
-            }
+            const int64_t tr = t < T ? t : 0;
+            select_in_segment<EP>(v, e, e < ne, k, renorm, t < T, topk_idx + tr * k,
+                                  topk_w + tr * k);
         }
     }
 }
