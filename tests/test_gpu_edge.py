@@ -1,6 +1,7 @@
 """Edge cases and properties of the layer on the GPU: a single token, one
-expert, k = E without renormalisation, every token on one expert, an empty
-batch, determinism, CUDA-graph capture, and the host-buffer entry point."""
+expert, k = E without renormalisation, every token on one expert, layers
+chained on one stream, an empty batch, determinism, CUDA-graph capture, and
+the host-buffer entry point."""
 import pytest
 import torch
 
@@ -99,6 +100,35 @@ def _layer(moe, name, T):
     layer = moe.MoELayer(inp["Wr"], inp["Wgu"], inp["Wd"], w.k,
                          None if inp["bias"] is None else inp["bias"], w.renorm)
     return layer, inp["x"]
+
+
+@pytest.mark.parametrize("name,T,f", [("mixtral", 4096, 3584),     # rows copied: one-launch dispatch
+                                      ("qwen3_zipf", 4096, 768)])  # rows gathered in G1
+def test_layers_chained_on_one_stream(moe, name, T, f):
+    """Each call takes as its x the output that the previous call's combine
+    has just written on the same stream.  The layer's kernels are scheduled
+    before their predecessors finish (programmatic dependent launch) but
+    read nothing before their wait, so four calls of two alternating layers
+    queued with no synchronisation equal, bit for bit, the same chain with a
+    device synchronisation after every call."""
+    ws = [synth.WORKLOADS[name].with_(T=T, f=f, seed=s) for s in (11, 12)]
+    layers = []
+    for w in ws:
+        inp = synth.make_inputs(w, device="cuda")
+        layers.append(moe.MoELayer(inp["Wr"], inp["Wgu"], inp["Wd"], w.k, inp["bias"], w.renorm))
+    x0 = synth.make_inputs(ws[0], device="cuda", weights=False)["x"]
+    ref = x0
+    for i in range(4):
+        ref = layers[i % 2](ref).clone()
+        torch.cuda.synchronize()
+    outs = [torch.empty_like(x0) for _ in range(4)]
+    cur = x0
+    for i in range(4):
+        layers[i % 2](cur, out=outs[i])
+        cur = outs[i]
+    torch.cuda.synchronize()
+    assert torch.equal(outs[-1], ref)
+    assert moe.moe_last_device_error(raise_on_error=False) == moe.MOE_OK
 
 
 def test_empty_batch(moe):
